@@ -1,0 +1,162 @@
+"""Seeded synthetic inputs for the attention kernels and for the CPU oracle.
+
+This module only draws and encodes inputs: it holds none of the attention
+arithmetic.  Both the CUDA path and the oracle receive exactly the tensors made
+here.  Rounding to bf16 and to e4m3 uses PyTorch's CPU casts (round to nearest
+even); the oracle decodes the resulting codes with its own decoder.
+
+Recipe (every workload, seed 0 unless the caller passes another seed):
+  * generator: NumPy ``default_rng(seed)`` (PCG64);
+  * draw order: decode sequence lengths (``integers(Lmin, Lmax + 1, B)``),
+    then Q, K, V as float32 ``standard_normal``, then outlier masks (one
+    ``random()`` draw per entry, outlier where < fraction), then rotation signs;
+  * outliers multiply single entries of the float32 draws before rounding;
+  * values are rounded to bf16 once.
+
+Workload shapes follow the attention problem statement of "Fast Inference and
+Training at Scale" §6.21 (Q, K, V of N x d_k per head) with grouped-query heads
+as in its §6.2 (h query heads, G key/value heads, h/G per group).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+TILE = 128  # FP8 scale tile: one fp32 scale per 128 rows x 128 columns
+
+# Named workloads.  ``S`` is Sq = Sk for prefill.
+WORKLOADS = {
+    "tiny": dict(kind="prefill", B=1, Hq=2, Hkv=2, S=128, D=64, causal=None),
+    "train_prefill_mha": dict(kind="prefill", B=4, Hq=32, Hkv=32, S=4096, D=128, causal=True),
+    "long_gqa_prefill": dict(kind="prefill", B=1, Hq=32, Hkv=8, S=16384, D=128, causal=True,
+                             k_outlier_frac=0.01, k_outlier_mult=20.0),
+    "gqa_decode": dict(kind="decode", B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192),
+    "fp8_prefill": dict(kind="fp8", B=2, Hq=16, Hkv=16, S=8192, D=128, causal=False,
+                        outlier_frac=0.005, outlier_mult=50.0),
+}
+
+
+def to_bf16(x: np.ndarray) -> torch.Tensor:
+    """Round a float32 array to bf16 (RNE) with PyTorch's CPU cast."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _apply_outliers(rng, x: np.ndarray, frac: float, mult: float) -> None:
+    mask = rng.random(x.shape, dtype=np.float32) < frac
+    x[mask] *= mult
+
+
+def make_prefill(B, Hq, Hkv, Sq, Sk, D, seed=0, k_outlier_frac=0.0, k_outlier_mult=1.0):
+    """bf16 Q [B,Hq,Sq,D], K and V [B,Hkv,Sk,D], entries N(0,1).
+
+    With ``k_outlier_frac`` > 0, that fraction of K's entries (i.i.d. per entry)
+    is multiplied by ``k_outlier_mult`` before rounding.
+    """
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, Sq, D), dtype=np.float32)
+    k = rng.standard_normal((B, Hkv, Sk, D), dtype=np.float32)
+    v = rng.standard_normal((B, Hkv, Sk, D), dtype=np.float32)
+    if k_outlier_frac > 0:
+        _apply_outliers(rng, k, k_outlier_frac, k_outlier_mult)
+    return dict(q=to_bf16(q), k=to_bf16(k), v=to_bf16(v))
+
+
+def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True):
+    """One query token per sequence against a contiguous per-sequence KV cache.
+
+    Returns q [B,Hq,D] bf16, kcache/vcache [B,Hkv,Lmax,D] bf16 and seqlens [B]
+    int32 drawn uniformly in [Lmin, Lmax].  Cache rows at or beyond a
+    sequence's length are set to NaN when ``poison_tail`` so that any read of
+    them shows up in the output.
+    """
+    rng = np.random.default_rng(seed)
+    seqlens = rng.integers(Lmin, Lmax + 1, size=B).astype(np.int32)
+    q = rng.standard_normal((B, Hq, D), dtype=np.float32)
+    k = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
+    v = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
+    if poison_tail:
+        pos = np.arange(Lmax)[None, None, :, None]
+        dead = pos >= seqlens[:, None, None, None]
+        dead = np.broadcast_to(dead, k.shape)
+        k[dead] = np.nan
+        v[dead] = np.nan
+    return dict(q=to_bf16(q), kcache=to_bf16(k), vcache=to_bf16(v),
+                seqlens=torch.from_numpy(seqlens))
+
+
+def hadamard(n: int) -> np.ndarray:
+    """Sylvester Hadamard matrix of order n (a power of two), entries +-1."""
+    assert n > 0 and (n & (n - 1)) == 0
+    h = np.ones((1, 1), dtype=np.float64)
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def rotation(D: int, signs: np.ndarray) -> np.ndarray:
+    """Random orthogonal matrix R = H_D . diag(signs) / sqrt(D), float64."""
+    return hadamard(D) * signs[None, :].astype(np.float64) / math.sqrt(D)
+
+
+def quantize_tiles_e4m3(x: torch.Tensor, tile: int = TILE):
+    """Block quantisation: one fp32 scale per tile x tile block of each (b, h) matrix.
+
+    x: float32 [B, H, S, D].  scale = amax / 448 (1 where a block is all zero);
+    code = e4m3(x / scale), rounded to nearest even by PyTorch's cast.
+    Returns (codes uint8 [B,H,S,D], scales float32 [B,H,ceil(S/tile),ceil(D/tile)]).
+    """
+    B, H, S, D = x.shape
+    nt_s, nt_d = -(-S // tile), -(-D // tile)
+    pad = torch.zeros(B, H, nt_s * tile, nt_d * tile, dtype=torch.float32)
+    pad[:, :, :S, :D] = x
+    blocks = pad.view(B, H, nt_s, tile, nt_d, tile)
+    amax = blocks.abs().amax(dim=(3, 5))
+    scales = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+    scaled = blocks / scales[:, :, :, None, :, None]
+    scaled = scaled.clamp(-448.0, 448.0)
+    codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = codes.view(B, H, nt_s * tile, nt_d * tile)[:, :, :S, :D].contiguous()
+    return codes, scales.contiguous()
+
+
+def make_fp8_prefill(B, Hq, Hkv, Sq, Sk, D, seed=0, outlier_frac=0.005, outlier_mult=50.0):
+    """FP8 e4m3 inputs with one fp32 scale per 128 x 128 tile.
+
+    bf16 N(0,1) draws with ``outlier_frac`` of the entries of each of Q, K, V
+    multiplied by ``outlier_mult``; Q and K are then multiplied (as row vectors)
+    by one seeded rotation R = H_D diag(s) / sqrt(D) in float32, which leaves
+    Q K^T unchanged; V is not rotated.  All three are then block-quantised.
+    """
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, Sq, D), dtype=np.float32)
+    k = rng.standard_normal((B, Hkv, Sk, D), dtype=np.float32)
+    v = rng.standard_normal((B, Hkv, Sk, D), dtype=np.float32)
+    for x in (q, k, v):
+        _apply_outliers(rng, x, outlier_frac, outlier_mult)
+    signs = rng.integers(0, 2, size=D).astype(np.float64) * 2.0 - 1.0
+    R = torch.from_numpy(rotation(D, signs).astype(np.float32))
+    qb, kb, vb = to_bf16(q).float(), to_bf16(k).float(), to_bf16(v).float()
+    qr = (qb.reshape(-1, D) @ R).reshape(qb.shape)
+    kr = (kb.reshape(-1, D) @ R).reshape(kb.shape)
+    q8, qs = quantize_tiles_e4m3(qr)
+    k8, ks = quantize_tiles_e4m3(kr)
+    v8, vs = quantize_tiles_e4m3(vb)
+    return dict(q8=q8, k8=k8, v8=v8, q_scale=qs, k_scale=ks, v_scale=vs, signs=signs)
+
+
+def make_workload(name: str, seed: int = 0, **override):
+    """Inputs for a named workload (see ``WORKLOADS``)."""
+    cfg = dict(WORKLOADS[name])
+    cfg.update(override)
+    kind = cfg["kind"]
+    if kind == "prefill":
+        return make_prefill(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["S"], cfg["D"], seed,
+                            cfg.get("k_outlier_frac", 0.0), cfg.get("k_outlier_mult", 1.0))
+    if kind == "decode":
+        return make_decode(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Lmin"], cfg["Lmax"], seed)
+    if kind == "fp8":
+        return make_fp8_prefill(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["S"], cfg["D"], seed,
+                                cfg["outlier_frac"], cfg["outlier_mult"])
+    raise ValueError(kind)

@@ -1,0 +1,293 @@
+"""Pins of the CPU fp64 oracle against what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped rescale,
+a transposed operand, a wrong scale, a wrong GQA index, an off-by-one causal
+mask, a sign error in a codec) fails at least one of them.  All run on the CPU.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from exact_tiled_attention_15_gb300 import workloads
+
+TOL = 1e-12
+
+
+def rand(*shape, seed=0, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------- definition pins
+def test_identity_values_recover_softmax_rows():
+    """With V = I the output is P itself: rows are non-negative, sum to 1
+    ("each row sums to 1", Fast Inference §6.21) and P_ij / P_i0 equals
+    exp(scale * q_i.(k_j - k_0)) -- which fixes the scale and the operand order."""
+    Sq, Sk, D = 5, 9, 4
+    q, k = rand(1, 1, Sq, D, seed=1), rand(1, 1, Sk, D, seed=2)
+    v = np.eye(Sk)[None, None]
+    scale = 0.37
+    O, L = oracle.attention(q, k, v, scale=scale)
+    P = O[0, 0]
+    assert (P >= 0).all()
+    np.testing.assert_allclose(P.sum(1), 1.0, atol=TOL)
+    ratio = np.log(P / P[:, :1])
+    expect = scale * (q[0, 0] @ (k[0, 0] - k[0, 0, :1]).T)
+    np.testing.assert_allclose(ratio, expect, atol=1e-10)
+    # LSE makes exp(s_ij - LSE_i) sum to one
+    s = scale * q[0, 0] @ k[0, 0].T
+    np.testing.assert_allclose(np.exp(s - L[0, 0][:, None]).sum(1), 1.0, atol=TOL)
+
+
+def test_constant_values_give_constant_output():
+    """O is a convex combination of V rows, so V = c everywhere gives O = c."""
+    q, k = rand(2, 3, 17, 8, seed=3), rand(2, 3, 23, 8, seed=4)
+    v = np.full((2, 3, 23, 8), 2.5)
+    for causal in (False, True):
+        O, _ = oracle.attention(q, k, v, causal=causal)
+        np.testing.assert_allclose(O, 2.5, atol=TOL)
+
+
+def test_causal_first_row_is_first_value_row():
+    """Causal, Sq = Sk: query 0 sees key 0 only, so O_0 = V_0, LSE_0 = s_00."""
+    q, k, v = rand(1, 2, 16, 8, seed=5), rand(1, 2, 16, 8, seed=6), rand(1, 2, 16, 8, seed=7)
+    O, L = oracle.attention(q, k, v, causal=True, scale=0.5)
+    np.testing.assert_allclose(O[:, :, 0], v[:, :, 0], atol=TOL)
+    np.testing.assert_allclose(L[:, :, 0], 0.5 * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0]), atol=TOL)
+    # and the last row sees every key: equals the non-causal last row
+    On, Ln = oracle.attention(q, k, v, causal=False, scale=0.5)
+    np.testing.assert_allclose(O[:, :, -1], On[:, :, -1], atol=TOL)
+    np.testing.assert_allclose(L[:, :, -1], Ln[:, :, -1], atol=TOL)
+
+
+def test_causal_brute_force_prefix():
+    """Causal row i equals the non-causal result over keys 0..i + (Sk - Sq)."""
+    Sq, Sk, D = 6, 10, 4
+    q, k, v = rand(1, 1, Sq, D, seed=8), rand(1, 1, Sk, D, seed=9), rand(1, 1, Sk, D, seed=10)
+    O, L = oracle.attention(q, k, v, causal=True)
+    for i in range(Sq):
+        n = i + (Sk - Sq) + 1
+        Oi, Li = oracle.attention(q[:, :, i:i + 1], k[:, :, :n], v[:, :, :n], causal=False)
+        np.testing.assert_allclose(O[:, :, i], Oi[:, :, 0], atol=TOL)
+        np.testing.assert_allclose(L[:, :, i], Li[:, :, 0], atol=TOL)
+
+
+@pytest.mark.parametrize("form", ["per_step", "deferred"])
+@pytest.mark.parametrize("block", [1, 7, 64, 128, 300])
+@pytest.mark.parametrize("causal", [False, True])
+def test_online_softmax_matches_direct_computation(form, block, causal):
+    """The tiled online-softmax recurrence gives the same result for any block
+    size, in both the per-step and the deferred form (Hardware Co-Design;
+    Week 13 step 2: the block size does not matter)."""
+    q, k, v = rand(2, 4, 37, 16, seed=11), rand(2, 2, 300, 16, seed=12), rand(2, 2, 300, 16, seed=13)
+    O, L = oracle.attention(q, k, v, causal=causal)
+    O2, L2 = oracle.attention_online(q, k, v, causal=causal, block=block, form=form)
+    np.testing.assert_allclose(O2, O, rtol=1e-12, atol=TOL)
+    np.testing.assert_allclose(L2, L, rtol=1e-12, atol=TOL)
+
+
+def test_online_softmax_handles_large_logits():
+    """Huge logits overflow neither form, and the output goes to V_argmax
+    (Week 13, common mistakes)."""
+    q, k, v = rand(1, 1, 8, 16, seed=14, scale=1e4), rand(1, 1, 64, 16, seed=15), rand(1, 1, 64, 16, seed=16)
+    O, L = oracle.attention(q, k, v)
+    assert np.isfinite(O).all() and np.isfinite(L).all()
+    s = q[0, 0] @ k[0, 0].T / 4.0
+    top = s.argmax(1)
+    gap = np.sort(s, 1)[:, -1] - np.sort(s, 1)[:, -2]
+    assert (gap > 50).all()
+    np.testing.assert_allclose(O[0, 0], v[0, 0][top], atol=1e-12)
+    for form in ("per_step", "deferred"):
+        O2, L2 = oracle.attention_online(q, k, v, block=5, form=form)
+        np.testing.assert_allclose(O2, O, atol=1e-9)
+        np.testing.assert_allclose(L2, L, rtol=1e-12)
+
+
+def test_fully_masked_rows_are_zero_not_nan():
+    """Causal with Sq > Sk: the first Sq - Sk rows have no key.  They come out
+    as O = 0, LSE = -inf, with no NaN (m = -inf must not give e^(-inf+inf))."""
+    q, k, v = rand(1, 1, 12, 8, seed=17), rand(1, 1, 5, 8, seed=18), rand(1, 1, 5, 8, seed=19)
+    for fn in (oracle.attention, lambda *a, **kw: oracle.attention_online(*a, block=2, **kw)):
+        O, L = fn(q, k, v, causal=True)
+        assert not np.isnan(O).any() and not np.isnan(L).any()
+        np.testing.assert_array_equal(O[0, 0, :7], 0.0)
+        assert np.isneginf(L[0, 0, :7]).all()
+        assert np.isfinite(L[0, 0, 7:]).all()
+        np.testing.assert_allclose(O[0, 0, 7], v[0, 0, 0], atol=TOL)
+
+
+def test_gqa_equals_mha_on_repeated_heads():
+    """GQA with Hkv < Hq equals MHA on K, V repeated per group (contiguous
+    groups, Fast Inference §6.2); Hkv = 1 is MQA; Hkv = Hq is MHA."""
+    B, Hq, S, D = 2, 8, 19, 8
+    q = rand(B, Hq, S, D, seed=20)
+    for Hkv in (8, 4, 2, 1):
+        k, v = rand(B, Hkv, S, D, seed=21), rand(B, Hkv, S, D, seed=22)
+        g = Hq // Hkv
+        kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+        for causal in (False, True):
+            O, L = oracle.attention(q, k, v, causal=causal)
+            Om, Lm = oracle.attention(q, kr, vr, causal=causal)
+            np.testing.assert_array_equal(O, Om)
+            np.testing.assert_array_equal(L, Lm)
+    # a head's result depends on its own group's K/V only: perturbing group 1
+    # must not move heads of group 0
+    k, v = rand(B, 2, S, D, seed=23), rand(B, 2, S, D, seed=24)
+    O1, _ = oracle.attention(q, k, v)
+    k2 = k.copy()
+    k2[:, 1] += rand(B, S, D, seed=99)
+    O2, _ = oracle.attention(q, k2, v)
+    np.testing.assert_array_equal(O1[:, :4], O2[:, :4])
+    assert np.abs(O1[:, 4:] - O2[:, 4:]).max() > 1e-3
+
+
+def test_closed_forms():
+    """Q = 0: uniform weights, O = mean of allowed V rows, LSE = ln(#allowed).
+    Sk = 1: O = V_0.  Sk = 2: logistic weights, LSE = logaddexp."""
+    Sq, Sk, D = 6, 6, 4
+    v = rand(1, 1, Sk, D, seed=25)
+    q = np.zeros((1, 1, Sq, D))
+    k = rand(1, 1, Sk, D, seed=26)
+    O, L = oracle.attention(q, k, v, causal=True)
+    for i in range(Sq):
+        np.testing.assert_allclose(O[0, 0, i], v[0, 0, :i + 1].mean(0), atol=TOL)
+        np.testing.assert_allclose(L[0, 0, i], math.log(i + 1), atol=TOL)
+    q1 = rand(1, 1, 3, D, seed=27)
+    O, L = oracle.attention(q1, k[:, :, :1], v[:, :, :1])
+    np.testing.assert_allclose(O[0, 0], np.repeat(v[0, 0, :1], 3, 0), atol=TOL)
+    O, L = oracle.attention(q1, k[:, :, :2], v[:, :, :2], scale=0.8)
+    s = 0.8 * q1[0, 0] @ k[0, 0, :2].T
+    w0 = 1.0 / (1.0 + np.exp(s[:, 1] - s[:, 0]))
+    np.testing.assert_allclose(O[0, 0], w0[:, None] * v[0, 0, 0] + (1 - w0)[:, None] * v[0, 0, 1], atol=TOL)
+    np.testing.assert_allclose(L[0, 0], np.logaddexp(s[:, 0], s[:, 1]), atol=TOL)
+
+
+def test_key_permutation_invariance():
+    """Without a mask, permuting keys and values together leaves O unchanged."""
+    q, k, v = rand(1, 2, 9, 8, seed=28), rand(1, 2, 31, 8, seed=29), rand(1, 2, 31, 8, seed=30)
+    perm = np.random.default_rng(31).permutation(31)
+    O, L = oracle.attention(q, k, v)
+    O2, L2 = oracle.attention(q, k[:, :, perm], v[:, :, perm])
+    np.testing.assert_allclose(O2, O, atol=TOL)
+    np.testing.assert_allclose(L2, L, atol=TOL)
+
+
+def test_split_merge_equals_full():
+    """Attention over disjoint key chunks, merged by log-sum-exp weights, equals
+    attention over all keys (the merge a split-K decode uses)."""
+    q, k, v = rand(2, 4, 3, 16, seed=32), rand(2, 4, 200, 16, seed=33), rand(2, 4, 200, 16, seed=34)
+    O, L = oracle.attention(q, k, v)
+    cuts = [0, 1, 50, 51, 133, 200]
+    parts = [oracle.attention(q, k[:, :, a:b], v[:, :, a:b]) for a, b in zip(cuts[:-1], cuts[1:])]
+    Om, Lm = oracle.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+    np.testing.assert_allclose(Om, O, atol=TOL)
+    np.testing.assert_allclose(Lm, L, atol=TOL)
+    # an empty chunk (lse = -inf) changes nothing
+    Oe, Le = oracle.merge_partials([parts[0][0], np.zeros_like(O)], [parts[0][1], np.full_like(L, -np.inf)])
+    np.testing.assert_allclose(Oe, parts[0][0], atol=TOL)
+    np.testing.assert_allclose(Le, parts[0][1], atol=TOL)
+
+
+@pytest.mark.parametrize("Hq,Hkv,Sq,Sk,causal", [(4, 4, 33, 33, False), (4, 4, 33, 33, True),
+                                                 (8, 2, 20, 57, False), (6, 1, 40, 40, True)])
+def test_matches_library_sdpa(Hq, Hkv, Sq, Sk, causal):
+    """Library special case: PyTorch's CPU scaled_dot_product_attention in
+    float64 (test only; the oracle does not use it).  Its logsumexp comes
+    from the CPU flash kernel, which aligns the causal mask at the top left,
+    so LSE is compared where the two alignments coincide (Sq = Sk)."""
+    q, k, v = rand(2, Hq, Sq, 16, seed=35), rand(2, Hkv, Sk, 16, seed=36), rand(2, Hkv, Sk, 16, seed=37)
+    O, L = oracle.attention(q, k, v, causal=causal)
+    tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+    Ot = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, enable_gqa=True)
+    if not causal or Sq == Sk:
+        np.testing.assert_allclose(O, Ot.numpy(), atol=1e-10)
+        g = Hq // Hkv
+        _, lse = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(
+            tq, tk.repeat_interleave(g, 1), tv.repeat_interleave(g, 1), 0.0, causal)
+        np.testing.assert_allclose(L, lse.numpy(), atol=1e-10)
+
+
+def test_decode_matches_prefill_definition_and_ignores_tail():
+    """Decode is the Sq = 1 case over the first seqlens[b] cache rows; rows
+    beyond a sequence's length (NaN here) never reach the result."""
+    w = workloads.make_decode(B=3, Hq=8, Hkv=2, D=16, Lmin=1, Lmax=40, seed=3)
+    q = w["q"].double().numpy()
+    kc, vc = w["kcache"].double().numpy(), w["vcache"].double().numpy()
+    sl = w["seqlens"].numpy()
+    assert np.isnan(kc).any()
+    O, L = oracle.decode(q, kc, vc, sl)
+    assert np.isfinite(O).all() and np.isfinite(L).all()
+    for b in range(3):
+        n = sl[b]
+        Ob, Lb = oracle.attention(q[b:b + 1, :, None], kc[b:b + 1, :, :n], vc[b:b + 1, :, :n])
+        np.testing.assert_allclose(O[b], Ob[0, :, 0], atol=TOL)
+        np.testing.assert_allclose(L[b], Lb[0, :, 0], atol=TOL)
+        tq = torch.from_numpy(q[b:b + 1, :, None])
+        Ot = F.scaled_dot_product_attention(tq, torch.from_numpy(kc[b:b + 1, :, :n]),
+                                            torch.from_numpy(vc[b:b + 1, :, :n]), enable_gqa=True)
+        np.testing.assert_allclose(O[b], Ot[0, :, 0].numpy(), atol=1e-10)
+    # empty sequence
+    O0, L0 = oracle.decode(q[:1], kc[:1], vc[:1], np.array([0]))
+    assert (O0 == 0).all() and np.isneginf(L0).all()
+
+
+# ---------------------------------------------------------------- codecs
+def test_bf16_decoder_matches_library_cast():
+    codes = np.arange(1 << 16, dtype=np.uint16)
+    ours = oracle.bf16_decode(codes)
+    lib = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(ours)
+    np.testing.assert_array_equal(ours[ok], lib[ok])
+
+
+def test_e4m3_decoder_matches_library_cast_and_spec_points():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(ours)
+    np.testing.assert_array_equal(ours[ok], lib[ok])
+    assert ours[0x7E] == 448.0 and ours[0xFE] == -448.0          # largest finite
+    assert ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6    # smallest subnormal / normal
+    assert ours[0x38] == 1.0 and np.isnan(ours[0x7F]) and np.isnan(ours[0xFF])
+    assert np.isnan(ours).sum() == 2                             # no infinities, two NaNs
+
+
+def test_dequantize_tiles_matches_library_and_scale_layout():
+    w = workloads.make_fp8_prefill(B=1, Hq=2, Hkv=2, Sq=300, Sk=300, D=128, seed=4)
+    codes, scales = w["q8"], w["q_scale"]
+    assert scales.shape == (1, 2, 3, 1)
+    ours = oracle.dequantize_tiles(codes.numpy(), scales.numpy())
+    lib = codes.view(torch.float8_e4m3fn).double()
+    lib = lib * scales.double().repeat_interleave(128, 2)[:, :, :300].repeat_interleave(128, 3)[..., :128]
+    np.testing.assert_array_equal(ours, lib.numpy())
+    # each tile's largest magnitude lands on the top code (amax / scale = 448)
+    for t in range(3):
+        blk = np.abs(oracle.e4m3_decode(codes[0, 0, t * 128:(t + 1) * 128].numpy()))
+        assert blk.max() == 448.0
+
+
+# ---------------------------------------------------------------- input generator pins
+def test_rotation_is_orthogonal_and_preserves_scores():
+    """Incoherent processing (FlashAttention-3): rotating Q and K by the same
+    orthogonal R leaves Q K^T unchanged."""
+    signs = np.random.default_rng(0).integers(0, 2, 128) * 2.0 - 1.0
+    R = workloads.rotation(128, signs)
+    np.testing.assert_allclose(R @ R.T, np.eye(128), atol=1e-12)
+    q, k = rand(50, 128, seed=38), rand(60, 128, seed=39)
+    np.testing.assert_allclose((q @ R) @ (k @ R).T, q @ k.T, atol=1e-10)
+    H = workloads.hadamard(8)
+    np.testing.assert_array_equal(H @ H.T, 8 * np.eye(8))
+
+
+def test_decode_seqlens_recipe():
+    """Seed-0 decode workload: 64 lengths in [1024, 8192]; their sum fixes the
+    algorithmic KV bytes of the benchmark."""
+    rng = np.random.default_rng(0)
+    sl = rng.integers(1024, 8193, size=64)
+    assert sl.min() >= 1024 and sl.max() <= 8192
+    assert int(sl.sum()) == 299418
