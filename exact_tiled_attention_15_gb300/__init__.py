@@ -1,1 +1,12 @@
-"""Exact tiled attention for GB300 (sm_103a): Python binding of the C ABI."""
+"""Exact tiled attention for GB300 (sm_103a).
+
+    from exact_tiled_attention_15_gb300 import fwd, decode, fwd_fp8
+
+``fwd``      bf16 prefill (causal or not, MHA/GQA/MQA) -> (O, LSE)
+``decode``   one query token per sequence against a KV cache -> (O, LSE)
+``fwd_fp8``  FP8 e4m3 prefill with one scale per 128x128 tile -> (O, LSE)
+
+All three call the C ABI of libattn.so (include/attn.h) on the current CUDA
+stream; the library is loaded on first use and a missing library raises.
+"""
+from ._lib import AttnError, decode, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, version  # noqa: F401

@@ -1,0 +1,171 @@
+"""ctypes binding of the C ABI in include/attn.h.
+
+Argument marshalling only: PyTorch supplies device memory and the current
+stream, every step of the computation runs in the CUDA library.  There is no
+fallback: if libattn.so is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_NO_DEVICE"}
+
+# Every symbol the header declares, with (restype, argtypes).
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_get_error": (_I, [_P]),
+    "attn_status_str": (ctypes.c_char_p, [_I]),
+    "attn_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so once (after torch's CUDA runtime, so both share it)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"CUDA library {LIB_PATH} is not built; run "
+                        "`python -m exact_tiled_attention_15_gb300.build` (nvcc, sm_103a)")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != ATTN_OK:
+        raise AttnError(status, what)
+
+
+def _need(t, name, dtype, dims):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd(q, k, v, causal=False, scale=None, return_lse=True, out=None, lse_out=None):
+    """bf16 prefill forward.  q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] -> (o, lse)."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, Sk, D] matching q")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = out if out is not None else torch.empty_like(q)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                        1 if causal else 0, scale, _stream(q.device))
+    _check(st, "attn_fwd")
+    return o, lse
+
+
+def decode_workspace_bytes(B, Hq, Hkv, Lmax, D) -> int:
+    return int(lib().attn_decode_workspace_bytes(B, Hq, Hkv, Lmax, D))
+
+
+def decode(q, kcache, vcache, seqlens, scale=None, workspace=None, return_lse=True, out=None, lse_out=None):
+    """Decode: q [B,Hq,D] against cache [B,Hkv,Lmax,D] with seqlens [B] int32 -> (o, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kcache, "kcache", torch.bfloat16, 4)
+    _need(vcache, "vcache", torch.bfloat16, 4)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    B, Hq, D = q.shape
+    Hkv, Lmax = kcache.shape[1], kcache.shape[2]
+    if tuple(vcache.shape) != tuple(kcache.shape) or kcache.shape[0] != B or kcache.shape[3] != D:
+        raise ValueError("kcache and vcache must be [B, Hkv, Lmax, D] matching q")
+    if seqlens.shape[0] != B:
+        raise ValueError("seqlens must have B entries")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    nbytes = decode_workspace_bytes(B, Hq, Hkv, Lmax, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    o = out if out is not None else torch.empty_like(q)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    st = lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), _ptr(lse),
+                           B, Hq, Hkv, Lmax, D, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(q.device))
+    _check(st, "attn_decode")
+    return o, lse
+
+
+def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, return_lse=True):
+    """FP8 e4m3 prefill: codes (uint8) plus one fp32 scale per 128x128 tile -> (o bf16, lse)."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        _need(t, name, torch.uint8, 4)
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _need(t, name, torch.float32, 4)
+    B, Hq, Sq, D = q8.shape
+    Hkv, Sk = k8.shape[1], k8.shape[2]
+    if tuple(v8.shape) != tuple(k8.shape):
+        raise ValueError("k8 and v8 must have the same shape")
+    nt = lambda s: -(-s // 128)  # noqa: E731
+    if tuple(q_scale.shape) != (B, Hq, nt(Sq), nt(D)) or tuple(k_scale.shape) != (B, Hkv, nt(Sk), nt(D)) \
+            or tuple(v_scale.shape) != (B, Hkv, nt(Sk), nt(D)):
+        raise ValueError("scales must be [B, H, ceil(S/128), ceil(D/128)]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = torch.empty(B, Hq, Sq, D, device=q8.device, dtype=torch.bfloat16)
+    lse = torch.empty(B, Hq, Sq, device=q8.device, dtype=torch.float32) if return_lse else None
+    st = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                            _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, 1 if causal else 0, scale,
+                            _stream(q8.device))
+    _check(st, "attn_fwd_fp8")
+    return o, lse
+
+
+def get_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error word."""
+    return int(lib().attn_get_error(_stream(device)))
+
+
+def version() -> str:
+    return lib().attn_version().decode()

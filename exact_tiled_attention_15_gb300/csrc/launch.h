@@ -1,0 +1,52 @@
+// launch.h -- host-side launchers shared between the kernel translation units
+// and the C ABI layer (attn_api.cu).  Internal: not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace attn {
+
+// Keys per split of the decode kernel for these sizes (a multiple of 64).
+int decode_chunk(int B, int Hq, int Hkv, int Lmax);
+// Number of key splits for a cache of Lmax rows.
+inline int decode_nsplit(int Lmax, int chunk) { return (Lmax + chunk - 1) / chunk; }
+
+struct DecodeArgs {
+  const void *q;
+  const int32_t *seqlens;
+  void *o;
+  float *lse;
+  float *part_o;    // [B, Hq, nsplit, D]
+  float *part_lse;  // [B, Hq, nsplit], log2 domain
+  int B, Hq, Hkv, Lmax, D, chunk, nsplit;
+  float scale;
+  uint64_t timeout_ns;
+  unsigned *err;
+};
+
+// Launch split kernel + combine kernel.  tmap_k / tmap_v describe the caches as
+// 3-D tensors (D, Lmax, B*Hkv) with 64 x 64 boxes and 128-byte swizzle.
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                          cudaStream_t stream);
+
+struct FwdArgs {
+  void *o;
+  float *lse;
+  const float *q_scale, *k_scale, *v_scale;  // FP8 only
+  int B, Hq, Hkv, Sq, Sk, D, causal;
+  float scale;
+  uint64_t timeout_ns;
+  unsigned *err;
+};
+
+// bf16 prefill.  tmap_q/k/v: 3-D tensors (D, S, B*H) with 64 x 128 boxes, 128B swizzle.
+cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
+                            const CUtensorMap &tmap_v, cudaStream_t stream);
+
+// FP8 prefill.  tmap_q/k/v: 3-D tensors (D, S, B*H) of bytes with 128 x 128 boxes.
+cudaError_t launch_fwd_fp8(const FwdArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
+                           const CUtensorMap &tmap_v, cudaStream_t stream);
+
+}  // namespace attn

@@ -63,16 +63,18 @@ def make_prefill(B, Hq, Hkv, Sq, Sk, D, seed=0, k_outlier_frac=0.0, k_outlier_mu
     return dict(q=to_bf16(q), k=to_bf16(k), v=to_bf16(v))
 
 
-def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True):
+def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True, seqlens=None):
     """One query token per sequence against a contiguous per-sequence KV cache.
 
     Returns q [B,Hq,D] bf16, kcache/vcache [B,Hkv,Lmax,D] bf16 and seqlens [B]
-    int32 drawn uniformly in [Lmin, Lmax].  Cache rows at or beyond a
-    sequence's length are set to NaN when ``poison_tail`` so that any read of
-    them shows up in the output.
+    int32 drawn uniformly in [Lmin, Lmax] (or the given ``seqlens``, in which
+    case that draw is still made so the rest of the stream is unchanged).
+    Cache rows at or beyond a sequence's length are set to NaN when
+    ``poison_tail`` so that any read of them shows up in the output.
     """
     rng = np.random.default_rng(seed)
-    seqlens = rng.integers(Lmin, Lmax + 1, size=B).astype(np.int32)
+    drawn = rng.integers(Lmin, Lmax + 1, size=B).astype(np.int32)
+    seqlens = drawn if seqlens is None else np.asarray(seqlens, dtype=np.int32)
     q = rng.standard_normal((B, Hq, D), dtype=np.float32)
     k = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
     v = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)

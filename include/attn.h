@@ -1,0 +1,136 @@
+/*
+ * attn.h -- C ABI of the exact tiled attention library for GB300 (sm_103a).
+ *
+ * The operation (all entry points):  O = softmax(scale * Q K^T + mask) V, with
+ * the per-row log-sum-exp LSE_i = log sum_j exp(scale * q_i . k_j) over the
+ * allowed keys (natural log).  Problem statement: "Fast Inference and Training
+ * at Scale" §6.21 (the attention formula, Q, K, V of N x d_k); the method
+ * (tiles, running max / running sum, never writing the score matrix):
+ * the same section's "Idea 1", "Week 13. GPUs and FlashAttention" step 2 and
+ * "Hardware Co-Design" (FlashAttention section, the online-softmax update).
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers owned by the caller; the library keeps no
+ *     pointer after a call returns and allocates no device memory (the decode
+ *     workspace is passed in).
+ *   - Layouts are dense row-major ("contiguous"): Q/O [B, Hq, Sq, D],
+ *     K/V [B, Hkv, Sk, D], LSE [B, Hq, Sq].  Every tensor pointer must be
+ *     16-byte aligned.
+ *   - Grouped-query attention ("Fast Inference and Training at Scale" §6.2):
+ *     Hq must be a multiple of Hkv; query head h reads key/value head
+ *     h / (Hq / Hkv) (contiguous groups).  Hkv == Hq is MHA, Hkv == 1 is MQA.
+ *   - causal != 0 masks key j for query i unless j <= i + (Sk - Sq) (aligned at
+ *     the bottom right; plain j <= i when Sq == Sk).  A query row with no
+ *     allowed key gets O = 0 and LSE = -inf.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument errors are detected on the host before any
+ *     CUDA call and return a status without touching the GPU.  A launch
+ *     failure returns ATTN_ERR_CUDA.  Device-side faults of the pipeline (a
+ *     bounded wait that ran out) are recorded in a device error word that
+ *     attn_get_error() reads.
+ *   - The library is stateless apart from that error word and a per-device
+ *     cache of kernel attributes; calls may come from several host threads.
+ */
+#ifndef EXACT_TILED_ATTENTION_ATTN_H
+#define EXACT_TILED_ATTENTION_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, Hq % Hkv != 0 */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim other than 64/128) */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+  ATTN_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (reported by attn_get_error) */
+  ATTN_ERR_NO_DEVICE = 5    /* no usable sm_103 device for this call */
+} attn_status;
+
+/*
+ * attn_fwd -- bf16 prefill forward (causal or not, MHA/GQA/MQA).
+ *   q   [B, Hq,  Sq, D] bf16          o   [B, Hq, Sq, D] bf16 (written)
+ *   k,v [B, Hkv, Sk, D] bf16          lse [B, Hq, Sq] fp32 natural-log LSE
+ *                                         (written; may be NULL to skip)
+ *   B, Hq, Hkv, Sq, Sk >= 1; D in {64, 128} else ATTN_ERR_UNSUPPORTED;
+ *   scale > 0 and finite (usually 1/sqrt(D)).
+ * Arithmetic: bf16 products accumulated in fp32 by the tensor cores; softmax
+ * in fp32; the probabilities enter the P.V product rounded to bf16; O is
+ * divided by the fp32 row sum once at the end and rounded to bf16.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                     float scale, attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_bytes -- size in bytes of the scratch attn_decode needs
+ * for these sizes (partial outputs of the key splits).  0 on invalid sizes.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
+
+/*
+ * attn_decode -- one query token per sequence against a contiguous KV cache
+ * ("Fast Inference and Training at Scale" §6.1: the new token's query attends
+ * over every cached position, the cache already holding its own K and V).
+ *   q       [B, Hq, D] bf16            o   [B, Hq, D] bf16 (written)
+ *   kcache, vcache [B, Hkv, Lmax, D] bf16
+ *   seqlens [B] int32 device array, 0 <= seqlens[b] <= Lmax; rows at or beyond
+ *           seqlens[b] are never read into the result.  seqlens[b] == 0 gives
+ *           O = 0, LSE = -inf.  Values outside [0, Lmax] are clamped.
+ *   lse     [B, Hq] fp32 natural-log LSE (may be NULL)
+ *   workspace: device scratch of at least attn_decode_workspace_bytes(...)
+ *           bytes, 256-byte aligned; contents on entry do not matter; calls that
+ *           share one workspace must not overlap on the GPU.
+ *   Hq / Hkv <= 16 heads share a key/value head per block of work (larger
+ *   groups are split); D in {64, 128}.
+ * Keys are split into chunks processed in parallel, each with its own running
+ * max and sum; the partial results are merged with log-sum-exp weights.
+ */
+attn_status attn_decode(const void *q, const void *kcache, const void *vcache,
+                        const int32_t *seqlens, void *o, float *lse,
+                        int B, int Hq, int Hkv, int Lmax, int D, float scale,
+                        void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_fwd_fp8 -- FP8 e4m3 prefill forward with block quantisation
+ * ("FlashAttention scaling, multi-GPU training and weight quantization" §1,
+ * FlashAttention-3: FP8 tensor cores, tiles scaled independently).
+ *   q8 [B, Hq, Sq, D], k8/v8 [B, Hkv, Sk, D]: e4m3 codes (OCP E4M3, 1 byte).
+ *   q_scale [B, Hq,  ceil(Sq/128), ceil(D/128)] fp32, k_scale/v_scale
+ *   [B, Hkv, ceil(Sk/128), ceil(D/128)] fp32: the real value of element
+ *   (b,h,s,d) is e4m3(code) * scale[b,h,s/128,d/128].
+ *   o [B, Hq, Sq, D] bf16, lse [B, Hq, Sq] fp32 (may be NULL).
+ *   D == 128 only (one scale tile spans the head dimension).
+ * Scores are dequantised with one scalar per (query tile, key tile); the
+ * probabilities enter the P.V product as e4m3 with the value tile's scale
+ * folded in.
+ */
+attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                         const float *q_scale, const float *k_scale, const float *v_scale,
+                         void *o, float *lse, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                         int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_get_error -- synchronises `stream`, then returns and clears the device
+ * error word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a bounded
+ * pipeline wait ran out since the last call (its kernel then returned early
+ * and its outputs are invalid).  ATTN_ERR_CUDA if the synchronisation failed.
+ */
+attn_status attn_get_error(attn_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *attn_status_str(attn_status status);
+
+/* Library version string, e.g. "0.1.0". */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EXACT_TILED_ATTENTION_ATTN_H */

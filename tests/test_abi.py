@@ -1,0 +1,118 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+rejects bad arguments on the host before any CUDA work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_15_gb300 as eta
+from exact_tiled_attention_15_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+INVALID, UNSUPPORTED = 1, 2
+A = 0x10000  # a 16-byte aligned fake device address: never dereferenced by these calls
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s*(attn_[a-z_0-9]+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from exact_tiled_attention_15_gb300.build import build
+        build()
+    return eta.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"attn_fwd", "attn_decode", "attn_decode_workspace_bytes", "attn_fwd_fp8", "attn_get_error",
+            "attn_status_str", "attn_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+    assert set(declared_functions()) <= set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.attn_status_str(code).decode() == name
+    assert lib.attn_version().decode().count(".") == 2
+
+
+def p(x):
+    return ctypes.c_void_p(x)
+
+
+def fwd(lib, q=A, k=A, v=A, o=A, lse=None, B=1, Hq=2, Hkv=2, Sq=128, Sk=128, D=128, causal=0, scale=0.1):
+    return lib.attn_fwd(p(q), p(k), p(v), p(o), p(lse), B, Hq, Hkv, Sq, Sk, D, causal, scale, None)
+
+
+def test_fwd_rejects_bad_arguments_on_host(lib):
+    assert fwd(lib, q=0) == INVALID
+    assert fwd(lib, o=0) == INVALID
+    assert fwd(lib, Hq=3, Hkv=2) == INVALID
+    assert fwd(lib, B=0) == INVALID
+    assert fwd(lib, Sq=0) == INVALID
+    assert fwd(lib, Sk=-1) == INVALID
+    assert fwd(lib, scale=0.0) == INVALID
+    assert fwd(lib, scale=float("nan")) == INVALID
+    assert fwd(lib, scale=float("inf")) == INVALID
+    assert fwd(lib, k=A + 8) == INVALID          # misaligned for TMA
+    assert fwd(lib, lse=A + 2) == INVALID
+    assert fwd(lib, D=96) == UNSUPPORTED
+    assert fwd(lib, D=256) == UNSUPPORTED
+
+
+def fp8(lib, D=128, qs=A, Hq=2, Hkv=2):
+    return lib.attn_fwd_fp8(p(A), p(A), p(A), p(qs), p(A), p(A), p(A), None, 1, Hq, Hkv, 256, 256, D, 0, 0.1, None)
+
+
+def test_fp8_rejects_bad_arguments_on_host(lib):
+    assert fp8(lib, qs=0) == INVALID
+    assert fp8(lib, qs=A + 2) == INVALID
+    assert fp8(lib, Hq=4, Hkv=3) == INVALID
+    assert fp8(lib, D=64) == UNSUPPORTED
+
+
+def test_decode_workspace_and_validation(lib):
+    n = lib.attn_decode_workspace_bytes(64, 32, 8, 8192, 128)
+    assert n > 0 and n % 4 == 0
+    assert lib.attn_decode_workspace_bytes(0, 32, 8, 8192, 128) == 0
+    assert lib.attn_decode_workspace_bytes(2, 6, 4, 100, 128) == 0  # Hq % Hkv != 0
+    # workspace grows with Lmax and with the number of query heads
+    assert lib.attn_decode_workspace_bytes(64, 32, 8, 16384, 128) >= n
+    assert lib.attn_decode_workspace_bytes(64, 64, 8, 8192, 128) > n
+
+    def dec(ws=A, wsb=n, seq=A, D=128, Hq=32, Hkv=8, scale=0.1):
+        return lib.attn_decode(p(A), p(A), p(A), p(seq), p(A), None, 64, Hq, Hkv, 8192, D, scale, p(ws), wsb, None)
+
+    assert dec(ws=0) == INVALID
+    assert dec(wsb=n - 1) == INVALID
+    assert dec(ws=A + 16) == INVALID       # workspace must be 256-byte aligned
+    assert dec(seq=0) == INVALID
+    assert dec(seq=A + 1) == INVALID
+    assert dec(Hq=30) == INVALID
+    assert dec(scale=-1.0) == INVALID
+    m = lib.attn_decode_workspace_bytes(64, 32, 8, 8192, 80)
+    assert lib.attn_decode(p(A), p(A), p(A), p(A), p(A), None, 64, 32, 8, 8192, 80, 0.1, p(A), m, None) == UNSUPPORTED
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        eta.fwd(q, q, q)
+    with pytest.raises((TypeError, ValueError)):
+        eta.fwd(q.float(), q, q)
+    with pytest.raises(TypeError):
+        eta.fwd("q", q, q)

@@ -1,0 +1,93 @@
+"""GPU parity of the bf16 prefill kernel (tcgen05) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_15_gb300 import workloads
+from parity import check_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def run(B, Hq, Hkv, Sq, Sk, D, causal, seed=0, scale=None, mult=1.0, k_outlier=0.0):
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_prefill(B, Hq, Hkv, Sq, Sk, D, seed=seed, k_outlier_frac=k_outlier, k_outlier_mult=20.0)
+    if mult != 1.0:  # larger logits; V keeps its scale so the bound stays comparable
+        w = {n: (t.float() * mult).to(torch.bfloat16) if n in ("q", "k") else t for n, t in w.items()}
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, k, v, causal=causal, scale=scale)
+    assert eta.get_error() == 0
+    Or, Lr = oracle.attention(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                              causal=causal, scale=scale)
+    return check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr,
+                      what=f"fwd B{B} {Hq}/{Hkv} {Sq}x{Sk} D{D} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_config(causal):
+    """B=1, Hq=Hkv=2, S=128, D=64, fp32 N(0,1) draws from seed 0 rounded to bf16."""
+    run(1, 2, 2, 128, 128, 64, causal, seed=0)
+
+
+@pytest.mark.parametrize("S", [1, 100, 128, 129, 255, 256, 257, 600])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_square_shapes(S, D, causal):
+    run(1, 2, 2, S, S, D, causal, seed=S + D)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 1), (6, 3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_mqa(Hq, Hkv, causal):
+    run(2, Hq, Hkv, 300, 300, 128, causal, seed=Hq * 10 + Hkv)
+
+
+@pytest.mark.parametrize("Sq,Sk", [(100, 300), (1, 513), (300, 100), (129, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_unequal_lengths(Sq, Sk, causal):
+    """Sq != Sk: the causal mask aligns at the bottom right; with Sq > Sk the
+    first Sq - Sk rows see no key and must come out as O = 0, LSE = -inf."""
+    run(1, 4, 2, Sq, Sk, 128, causal, seed=Sq + Sk)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_logits_force_rescales(causal):
+    """Q and K x4 (scores 16x larger) make the running max move often, which
+    exercises the rescale of the TMEM accumulator."""
+    run(1, 2, 2, 700, 700, 128, causal, seed=11, mult=4.0)
+
+
+def test_k_outliers():
+    run(1, 4, 1, 512, 512, 128, True, seed=12, k_outlier=0.01)
+
+
+def _sampled(name, rows_per_head, heads, seed=0):
+    import exact_tiled_attention_15_gb300 as eta
+    cfg = workloads.WORKLOADS[name]
+    w = workloads.make_workload(name, seed=seed)
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, k, v, causal=cfg["causal"])
+    assert eta.get_error() == 0
+    o = o.cpu()
+    lse = lse.cpu()
+    S = cfg["S"]
+    rng = np.random.default_rng(1)
+    for (b, h) in heads:
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, S - 1],
+                                         rng.integers(0, S, rows_per_head)]))
+        Or, Lr = oracle.attention_rows(w["q"].double().numpy(), w["k"].double().numpy(),
+                                       w["v"].double().numpy(), b, h, rows, cfg["causal"], 1.0 / np.sqrt(cfg["D"]))
+        check_bf16(o[b, h, rows].double().numpy(), Or, lse[b, h, rows].numpy(), Lr, what=f"{name} b{b} h{h}")
+    assert torch.isfinite(o.float()).all()
+
+
+def test_train_prefill_full_size_sampled():
+    """B=4, 32/32 heads, S=4096, D=128, causal: sampled rows of 6 heads."""
+    _sampled("train_prefill_mha", 24, [(0, 0), (0, 31), (1, 7), (2, 16), (3, 30), (3, 31)])
+
+
+def test_long_gqa_prefill_full_size_sampled():
+    """B=1, 32/8 heads, S=16384, D=128, causal, 1% of K entries x20."""
+    _sampled("long_gqa_prefill", 12, [(0, 0), (0, 3), (0, 4), (0, 17), (0, 31)])
