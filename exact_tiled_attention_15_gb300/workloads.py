@@ -69,23 +69,27 @@ def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True, seqlens=Non
     Returns q [B,Hq,D] bf16, kcache/vcache [B,Hkv,Lmax,D] bf16 and seqlens [B]
     int32 drawn uniformly in [Lmin, Lmax] (or the given ``seqlens``, in which
     case that draw is still made so the rest of the stream is unchanged).
-    Cache rows at or beyond a sequence's length are set to NaN when
-    ``poison_tail`` so that any read of them shows up in the output.
+    Only the live cache rows (position < seqlens[b]) are drawn: first all of
+    K's, in (b, head, position, d) order, then all of V's.  Rows at or beyond a
+    sequence's length are NaN when ``poison_tail`` (so any read of them shows
+    up in the output), else 0.
     """
     rng = np.random.default_rng(seed)
     drawn = rng.integers(Lmin, Lmax + 1, size=B).astype(np.int32)
     seqlens = drawn if seqlens is None else np.asarray(seqlens, dtype=np.int32)
     q = rng.standard_normal((B, Hq, D), dtype=np.float32)
-    k = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
-    v = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
-    if poison_tail:
-        pos = np.arange(Lmax)[None, None, :, None]
-        dead = pos >= seqlens[:, None, None, None]
-        dead = np.broadcast_to(dead, k.shape)
-        k[dead] = np.nan
-        v[dead] = np.nan
-    return dict(q=to_bf16(q), kcache=to_bf16(k), vcache=to_bf16(v),
-                seqlens=torch.from_numpy(seqlens))
+    fill = np.nan if poison_tail else 0.0
+    caches = []
+    for _ in range(2):  # K, then V
+        c = torch.full((B, Hkv, Lmax, D), fill, dtype=torch.bfloat16)
+        live = rng.standard_normal(int(seqlens.sum()) * Hkv * D, dtype=np.float32)
+        off = 0
+        for b in range(B):
+            n = int(seqlens[b]) * Hkv * D
+            c[b, :, :seqlens[b]] = to_bf16(live[off:off + n].reshape(Hkv, int(seqlens[b]), D))
+            off += n
+        caches.append(c)
+    return dict(q=to_bf16(q), kcache=caches[0], vcache=caches[1], seqlens=torch.from_numpy(seqlens))
 
 
 def hadamard(n: int) -> np.ndarray:
