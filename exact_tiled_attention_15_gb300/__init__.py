@@ -9,4 +9,4 @@
 All three call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import AttnError, decode, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, version  # noqa: F401
+from ._lib import AttnError, decode, decode_noalloc, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, version  # noqa: F401

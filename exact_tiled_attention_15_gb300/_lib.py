@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libattn.so")
 
 ATTN_OK = 0
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
-          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_NO_DEVICE"}
+          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_NO_DEVICE", 6: "ATTN_ERR_SCRATCH_LIMIT"}
 
 # Every symbol the header declares, with (restype, argtypes).
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -26,6 +26,7 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_get_error": (_I, [_P]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
@@ -135,6 +136,31 @@ def decode(q, kcache, vcache, seqlens, scale=None, workspace=None, return_lse=Tr
                            B, Hq, Hkv, Lmax, D, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(q.device))
     _check(st, "attn_decode")
+    return o, lse
+
+
+def decode_noalloc(q, kcache, vcache, seqlens, scale=None, return_lse=True, out=None, lse_out=None):
+    """decode() for callers that cannot allocate device scratch: uses the
+    library's fixed 16 MiB static scratch (see attn_decode_noalloc in attn.h);
+    concurrent calls on one device must be serialised."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kcache, "kcache", torch.bfloat16, 4)
+    _need(vcache, "vcache", torch.bfloat16, 4)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    B, Hq, D = q.shape
+    Hkv, Lmax = kcache.shape[1], kcache.shape[2]
+    if tuple(vcache.shape) != tuple(kcache.shape) or kcache.shape[0] != B or kcache.shape[3] != D:
+        raise ValueError("kcache and vcache must be [B, Hkv, Lmax, D] matching q")
+    if seqlens.shape[0] != B:
+        raise ValueError("seqlens must have B entries")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = out if out is not None else torch.empty_like(q)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    st = lib().attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), _ptr(lse),
+                                   B, Hq, Hkv, Lmax, D, scale, _stream(q.device))
+    _check(st, "attn_decode_noalloc")
     return o, lse
 
 

@@ -110,6 +110,7 @@ const char *attn_status_str(attn_status s) {
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE";
+    case ATTN_ERR_SCRATCH_LIMIT: return "ATTN_ERR_SCRATCH_LIMIT";
   }
   return "ATTN_ERR_UNKNOWN";
 }

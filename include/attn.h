@@ -50,7 +50,8 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim other than 64/128) */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
   ATTN_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (reported by attn_get_error) */
-  ATTN_ERR_NO_DEVICE = 5    /* no usable sm_103 device for this call */
+  ATTN_ERR_NO_DEVICE = 5,   /* no usable sm_103 device for this call */
+  ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_decode_noalloc: sizes need more than its fixed scratch */
 } attn_status;
 
 /*
@@ -96,6 +97,36 @@ attn_status attn_decode(const void *q, const void *kcache, const void *vcache,
                         const int32_t *seqlens, void *o, float *lse,
                         int B, int Hq, int Hkv, int Lmax, int D, float scale,
                         void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* Size of the fixed device scratch array used by attn_decode_noalloc. */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/*
+ * attn_decode_noalloc -- attn_decode without a workspace argument; it
+ * allocates nothing.  (The pages have no counterpart of this call: it exists
+ * for callers, not for the method.)
+ *   For callers that cannot obtain device scratch: code handed only input and
+ *   output buffers (a custom-op or plugin interface with no workspace slot), or
+ *   a serving loop that must not call cudaMalloc, which may synchronise the
+ *   device.  No cudaMalloc, cudaFree or allocating library call is made.
+ *   Arguments, layouts, results and errors are those of attn_decode.  The
+ *   scratch is one static device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES
+ *   (16 MiB) that each GPU running this call keeps until the process exits.
+ *   Sizes whose attn_decode_workspace_bytes() exceeds it return
+ *   ATTN_ERR_SCRATCH_LIMIT before any GPU work.  The need is about
+ *   B * Hq * nsplit * (D + 1) * 4 bytes with nsplit ~ 4864 / (B * Hkv) key
+ *   splits (at most ceil(Lmax / 64)); e.g. 64 sequences, 32 query / 8 KV
+ *   heads, D = 128 need 10.1 MiB whatever Lmax is.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make it before any
+ *   stream capture.  All calls share the array: calls whose GPU work overlaps
+ *   race and return wrong results, so serialise them.  Nothing in the array
+ *   needs to start at zero.
+ */
+attn_status attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
+                                const int32_t *seqlens, void *o, float *lse,
+                                int B, int Hq, int Hkv, int Lmax, int D, float scale,
+                                attn_stream_t stream);
 
 /*
  * attn_fwd_fp8 -- FP8 e4m3 prefill forward with block quantisation
