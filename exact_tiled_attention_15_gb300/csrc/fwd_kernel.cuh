@@ -1,0 +1,479 @@
+// fwd_kernel.cuh -- prefill attention forward on the sm_103a tensor cores,
+// shared by the bf16 (fwd_bf16.cu) and FP8 e4m3 (fwd_fp8.cu) entry points.
+//
+// The method: "Fast Inference and Training at Scale" §6.21 (Idea 1, tiling):
+// Q is cut into row tiles and K, V into column tiles that live on chip; the
+// scores of one (Q tile, K tile) pair never reach HBM; a running max and a
+// running sum (the online softmax; update printed in "Hardware Co-Design",
+// FlashAttention section) stitch the tiles together, and only O (plus the
+// per-row log-sum-exp, "Week 13. GPUs and FlashAttention" step 2) is written.
+// The loop order is Q-outer / KV-inner and the grid spans (Q block, batch x
+// head), as FlashAttention-2 does ("FlashAttention scaling, multi-GPU
+// training and weight quantization" §1); division by the row sum is deferred
+// to the end; with a causal mask, key tiles wholly above the diagonal are
+// never visited (Week 13, step 2).  The FP8 variant follows FlashAttention-3
+// (same page, §1): e4m3 operands on the FP8 tensor cores with one scale per
+// 128 x 128 tile.
+//
+// GB300 mapping, one CTA = two 128-row Q tiles of one (batch, query head):
+//   warp 8      TMA producer: Q once, then K_j / V_j into 2-stage rings
+//               (cp.async.bulk.tensor, 128-byte swizzle, mbarrier tx counts);
+//   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T with tcgen05.mma
+//               (both operands in shared memory, fp32 accumulator in TMEM),
+//               then O_i += P_i V_j with P_i read from TMEM.  Issue order
+//               P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): while one Q tile's
+//               softmax runs, the tensor core works on the other tile;
+//   warps 0-3   softmax of Q tile 0, one thread per query row (TMEM lane);
+//   warps 4-7   softmax of Q tile 1.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it.
+// P_i overwrites the first columns of S_i.  The running max only moves when
+// the new maximum exceeds it by more than a threshold (log2 units), so O is
+// rescaled rarely.
+//
+// FP8 specifics: S_ij is dequantised by one scalar sq_i * sk_j * scale;
+// probabilities are multiplied by 2^4 * sv_j / max_j sv_j before the e4m3
+// rounding (so they stay in e4m3's normal range and carry the value tile's
+// scale), and the output is multiplied back by max_j sv_j / 2^4.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <math_constants.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace fwd {
+
+constexpr int BM = 128;          // query rows per Q tile
+constexpr int BN = 128;          // keys per K/V tile
+constexpr int NQT = 2;           // Q tiles per CTA
+constexpr int NSTAGE = 2;        // K and V ring depth
+constexpr int HALF = 128 * 128;  // 128 rows x 128 bytes: one 128-byte-swizzled slab of a tile
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int THREADS = 10 * 32;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct Bf16 {
+  static constexpr bool kFp8 = false;
+  static constexpr int kElem = 1 * 2;  // bytes per element
+  static constexpr int kMmaK = 16;     // K elements per MMA instruction (32 bytes)
+  static constexpr float kThresh = 8.f;  // lazy-rescale threshold, log2 units
+  static constexpr float kPre = 0.f;     // log2 of the probability pre-scale
+  static constexpr uint32_t kTypeBits = (1u << 7) | (1u << 10);  // A and B bf16
+};
+
+struct Fp8 {
+  static constexpr bool kFp8 = true;
+  static constexpr int kElem = 1;
+  static constexpr int kMmaK = 32;
+  static constexpr float kThresh = 4.f;
+  static constexpr float kPre = 4.f;
+  static constexpr uint32_t kTypeBits = 0u;  // A and B e4m3
+};
+
+template <class T, int D>
+struct Cfg {
+  static constexpr int NH = D * T::kElem / 128;  // 128-byte slabs per row
+  static constexpr int TILE = NH * HALF;         // one 128 x D tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQT * TILE;
+  static constexpr int OFF_V = OFF_K + NSTAGE * TILE;
+  static constexpr int OFF_BAR = OFF_V + NSTAGE * TILE;
+  static constexpr int NBAR = 1 + 4 * NSTAGE + 3 * NQT + 1;
+  static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
+  static constexpr int P_REGS = BN * T::kElem / 4;  // 32-bit TMEM columns holding one P row
+  __device__ static constexpr uint32_t col_s(int i) { return (uint32_t)(i * BN); }
+  __device__ static constexpr uint32_t col_o(int i) { return (uint32_t)(NQT * BN + i * D); }
+  // instruction descriptors: f32 accumulate, M = 128; V (B of P.V) is MN-major
+  static constexpr uint32_t IDESC_QK =
+      (1u << 4) | T::kTypeBits | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  static constexpr uint32_t IDESC_PV =
+      (1u << 4) | T::kTypeBits | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  static_assert(NH >= 1, "tile rows must span at least one 128-byte slab");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(NQT * BN + NQT * D <= (int)TMEM_COLS, "TMEM budget");
+};
+
+struct Params {
+  __nv_bfloat16 *o;
+  float *lse;
+  const float *q_scale, *k_scale, *v_scale;  // FP8 only
+  int B, Hq, Hkv, Sq, Sk, causal, g, nqb, nqt, nkt;
+  float scale_log2;
+  uint64_t timeout_ns;
+  unsigned *err;
+};
+
+template <class T>
+__device__ __forceinline__ void mma_qk(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (T::kFp8) mma_ss_f8(d, a, b, idesc, acc);
+  else mma_ss(d, a, b, idesc, acc);
+}
+
+template <class T>
+__device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (T::kFp8) mma_ts_f8(d, a_tmem, b, idesc, acc);
+  else mma_ts(d, a_tmem, b, idesc, acc);
+}
+
+template <class T, int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+               const __grid_constant__ CUtensorMap tmv, Params p) {
+  using C = Cfg<T, D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *q_full = bars;
+  uint64_t *k_full = bars + 1, *k_empty = k_full + NSTAGE;
+  uint64_t *v_full = k_empty + NSTAGE, *v_empty = v_full + NSTAGE;
+  uint64_t *s_full = v_empty + NSTAGE, *p_full = s_full + NQT, *o_full = p_full + NQT;
+  uint64_t *done_bar = o_full + NQT;
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
+
+  const int bh = blockIdx.y;  // b * Hq + hq
+  const int b = bh / p.Hq, hq = bh % p.Hq;
+  const int hkv = hq / p.g;
+  const int q0 = (p.nqb - 1 - (int)blockIdx.x) * (NQT * BM);  // latest (heaviest) query blocks first
+  const int off = p.Sk - p.Sq;                                 // causal alignment: key j <= row + off
+  // key tiles each Q tile visits (a prefix 0 .. nkv_t[i]-1)
+  int nkv_t[NQT];
+#pragma unroll
+  for (int i = 0; i < NQT; ++i) {
+    const int first = q0 + i * BM, last = min(first + BM - 1, p.Sq - 1);
+    int end = p.Sk;
+    if (last < first) end = 0;  // the tile lies past the last query row
+    else if (p.causal) end = min(p.Sk, last + off + 1);
+    nkv_t[i] = end > 0 ? (end + BN - 1) / BN : 0;
+  }
+  const int nkv = max(nkv_t[0], nkv_t[1]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (nkv == 0) {  // no query row of this block may attend to any key
+    if (threadIdx.x < NQT * BM) {
+      const int row = q0 + threadIdx.x;
+      if (row < p.Sq) {
+        uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + row) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        if (p.lse) p.lse[(size_t)bh * p.Sq + row] = -CUDART_INF_F;
+      }
+    }
+    return;
+  }
+
+  if (warp == WARP_MMA) {
+    tmem_alloc(tmem_ptr, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < NQT; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], BM);
+      mbar_init(&o_full[i], 1);
+    }
+    mbar_init(done_bar, 1);
+    mbar_init_fence();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == WARP_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_arrive_expect_tx(q_full, NQT * C::TILE);
+#pragma unroll
+      for (int i = 0; i < NQT; ++i)
+#pragma unroll
+        for (int h = 0; h < C::NH; ++h)
+          tma_load_3d(smem + C::OFF_Q + i * C::TILE + h * HALF, &tmq, q_full, h * (128 / T::kElem), q0 + i * BM,
+                      bh);
+      const int zk = b * p.Hkv + hkv;
+      int nk = 0, nv = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int slot = j % NSTAGE;
+        const uint32_t par = ((j / NSTAGE) - 1) & 1;
+        if (j >= NSTAGE && !mbar_wait(&k_empty[slot], par, p.timeout_ns, p.err)) break;
+        mbar_arrive_expect_tx(&k_full[slot], C::TILE);
+#pragma unroll
+        for (int h = 0; h < C::NH; ++h)
+          tma_load_3d(smem + C::OFF_K + slot * C::TILE + h * HALF, &tmk, &k_full[slot], h * (128 / T::kElem),
+                      j * BN, zk);
+        nk = j + 1;
+        if (j >= NSTAGE && !mbar_wait(&v_empty[slot], par, p.timeout_ns, p.err)) break;
+        mbar_arrive_expect_tx(&v_full[slot], C::TILE);
+#pragma unroll
+        for (int h = 0; h < C::NH; ++h)
+          tma_load_3d(smem + C::OFF_V + slot * C::TILE + h * HALF, &tmv, &v_full[slot], h * (128 / T::kElem),
+                      j * BN, zk);
+        nv = j + 1;
+      }
+      // Leave only once every copy issued here has landed.
+      mbar_wait(q_full, 0, p.timeout_ns, p.err);
+      for (int t = max(0, nk - NSTAGE); t < nk; ++t)
+        mbar_wait(&k_full[t % NSTAGE], (t / NSTAGE) & 1, p.timeout_ns, p.err);
+      for (int t = max(0, nv - NSTAGE); t < nv; ++t)
+        mbar_wait(&v_full[t % NSTAGE], (t / NSTAGE) & 1, p.timeout_ns, p.err);
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t qs = smem_u32(smem + C::OFF_Q), ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V);
+      // S_i = Q_i K_j^T: K-major operands, 32 bytes of the head dimension per instruction
+      auto issue_s = [&](int i, int j) {
+        const int slot = j % NSTAGE;
+#pragma unroll
+        for (int kk = 0; kk < D / T::kMmaK; ++kk) {
+          const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
+          mma_qk<T>(tmem + C::col_s(i), sdesc_sw128(qs + i * C::TILE + o, 16, 1024),
+                    sdesc_sw128(ks + slot * C::TILE + o, 16, 1024), C::IDESC_QK, kk > 0);
+        }
+        tc_commit(&s_full[i]);
+      };
+      // O_i += P_i V_j: P from TMEM (8 columns per instruction), V MN-major
+      // (rows = keys; 128-byte slabs of the head dimension HALF bytes apart)
+      auto issue_pv = [&](int i, int j) -> bool {
+        if (!mbar_wait(&p_full[i], j & 1, p.timeout_ns, p.err)) return false;
+        tc_fence_after();
+        const int slot = j % NSTAGE;
+#pragma unroll
+        for (int kk = 0; kk < BN / T::kMmaK; ++kk)
+          mma_pv<T>(tmem + C::col_o(i), tmem + C::col_s(i) + kk * 8,
+                    sdesc_sw128(vs + slot * C::TILE + kk * T::kMmaK * 128, HALF, 1024), C::IDESC_PV,
+                    (j > 0 || kk > 0));
+        tc_commit(&o_full[i]);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, p.timeout_ns, p.err) && mbar_wait(&k_full[0], 0, p.timeout_ns, p.err);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < NQT; ++i)
+          if (nkv_t[i] > 0) issue_s(i, 0);
+        tc_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int slot = j % NSTAGE;
+        const bool next = j + 1 < nkv;
+        if (!mbar_wait(&v_full[slot], (j / NSTAGE) & 1, p.timeout_ns, p.err)) break;
+        tc_fence_after();
+        if (j < nkv_t[0] && !issue_pv(0, j)) break;
+        if (next) {
+          if (!mbar_wait(&k_full[(j + 1) % NSTAGE], ((j + 1) / NSTAGE) & 1, p.timeout_ns, p.err)) break;
+          tc_fence_after();
+          if (j + 1 < nkv_t[0]) issue_s(0, j + 1);
+        }
+        if (j < nkv_t[1] && !issue_pv(1, j)) break;
+        tc_commit(&v_empty[slot]);
+        if (next) {
+          if (j + 1 < nkv_t[1]) issue_s(1, j + 1);
+          tc_commit(&k_empty[(j + 1) % NSTAGE]);
+        }
+      }
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, p.timeout_ns, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int i = warp >> 2;               // Q tile
+    const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
+    const int row = q0 + i * BM + r;       // query row
+    const int my_nkv = nkv_t[i];
+    const uint32_t taddr = tmem + (((warp & 3) * 32) << 16);
+    const uint32_t s_col = C::col_s(i), o_col = C::col_o(i);
+    const int lim = p.causal ? min(p.Sk - 1, row + off) : p.Sk - 1;  // last key this row may see
+    const int zk = b * p.Hkv + hkv;
+    // FP8: per-tile dequantisation scalars; the largest V scale of the row block
+    float cq = 1.f, sv_ref = 1.f;
+    if constexpr (T::kFp8) {
+      cq = __ldg(&p.q_scale[(size_t)bh * p.nqt + (q0 + i * BM) / BM]);
+      float mv = 0.f;
+      for (int j = lane; j < nkv; j += 32) mv = fmaxf(mv, __ldg(&p.v_scale[(size_t)zk * p.nkt + j]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+      sv_ref = fmaxf(mv, 1e-30f);
+    }
+    float m_use = -CUDART_INF_F;  // running max in log2 units (moved lazily)
+    float l = 0.f;                // running sum relative to m_use
+    bool ok = true;
+    for (int j = 0; j < my_nkv; ++j) {
+      float cj = p.scale_log2, e_off = T::kPre;
+      if constexpr (T::kFp8) {
+        cj *= cq * __ldg(&p.k_scale[(size_t)zk * p.nkt + j]);
+        e_off += __log2f(fmaxf(__ldg(&p.v_scale[(size_t)zk * p.nkt + j]), 1e-30f) / sv_ref);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i], j & 1, p.timeout_ns, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld128(taddr + s_col, s);
+      const int kb = j * BN;
+      if (kb + BN - 1 > lim) {  // diagonal or ragged tile: mask keys past lim
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (kb + e > lim) s[e] = __float_as_uint(-CUDART_INF_F);
+      }
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+      for (int e = 8; e < 128; e += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[e + u]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_new = fmaxf(m_use, mx * cj);
+      float alpha = 1.f;
+      const bool moved = m_new > m_use + T::kThresh;  // also true on the first finite max
+      // O holds earlier tiles' sums only once the max was finite; alpha may
+      // then underflow to exactly 0 (a jump of > 126 in log2 units), and O
+      // must still be multiplied by it.
+      const bool rescale_o = moved && j > 0 && m_use != -CUDART_INF_F;
+      if (moved) {
+        alpha = fast_exp2(m_use - m_new);  // 0 if nothing accumulated yet
+        m_use = m_new;
+      }
+      const float bias = e_off - ((m_use == -CUDART_INF_F) ? 0.f : m_use);
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[C::P_REGS];
+      if constexpr (T::kFp8) {
+#pragma unroll
+        for (int e = 0; e < 128; e += 4) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[e]), cj, bias));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cj, bias));
+          const float p2 = fast_exp2(fmaf(__uint_as_float(s[e + 2]), cj, bias));
+          const float p3 = fast_exp2(fmaf(__uint_as_float(s[e + 3]), cj, bias));
+          rs4[0] += p0;
+          rs4[1] += p1;
+          rs4[2] += p2;
+          rs4[3] += p3;
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
+          pk[e / 4] = lo | (hi << 16);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 128; e += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[e]), cj, bias));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cj, bias));
+          rs4[(e >> 1) & 3] += p0 + p1;
+          pk[e / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      l = l * alpha + (T::kFp8 ? rs * fast_exp2(-e_off) : rs);
+#pragma unroll
+      for (int c = 0; c < C::P_REGS / 32; ++c) {
+        uint32_t chunk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) chunk[e] = pk[c * 32 + e];
+        tmem_st32(taddr + s_col + c * 32, chunk);
+      }
+      // Rescale O_i by alpha once P_{j-1} V_{j-1} has landed (warp-uniform).
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.timeout_ns, p.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(taddr + o_col + c * 32, ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(taddr + o_col + c * 32, ov);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[i]);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[i], (my_nkv - 1) & 1, p.timeout_ns, p.err));
+    if (ok) {
+      tc_fence_after();
+      const float out_scale = T::kFp8 ? sv_ref * fast_exp2(-T::kPre) : 1.f;
+      const float inv = l > 0.f ? out_scale / l : 0.f;
+      uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + min(row, p.Sq - 1)) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        if (my_nkv > 0) {
+          tmem_ld32(taddr + o_col + c * 32, ov);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+        uint32_t pkd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pkd[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+        if (row < p.Sq) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            orow[c * 4 + e] = make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2], pkd[4 * e + 3]);
+        }
+      }
+      if (p.lse && row < p.Sq)
+        p.lse[(size_t)bh * p.Sq + row] = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <class T, int D>
+cudaError_t launch(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                   cudaStream_t st) {
+  using C = Cfg<T, D>;
+  Params p;
+  p.o = static_cast<__nv_bfloat16 *>(a.o);
+  p.lse = a.lse;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.causal = a.causal;
+  p.g = a.Hq / a.Hkv;
+  p.nqb = (a.Sq + NQT * BM - 1) / (NQT * BM);
+  p.nqt = (a.Sq + BM - 1) / BM;
+  p.nkt = (a.Sk + BN - 1) / BN;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.timeout_ns = a.timeout_ns;
+  p.err = a.err;
+  if ((long)a.B * a.Hq > 65535) return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.nqb, (unsigned)(a.B * a.Hq));
+  fwd_kernel<T, D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fwd
+}  // namespace attn

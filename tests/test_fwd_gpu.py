@@ -59,6 +59,25 @@ def test_large_logits_force_rescales(causal):
     run(1, 2, 2, 700, 700, 128, causal, seed=11, mult=4.0)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_jump_beyond_exp2_range(causal):
+    """Keys of the second and later tiles x60: the running max jumps by far
+    more than 126 (log2 units), so the rescale factor of the accumulated O
+    underflows to 0 and O must be zeroed, not kept."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_prefill(1, 2, 2, 400, 400, 128, seed=21)
+    k = w["k"].float()
+    k[:, :, 128:] *= 60.0
+    w["k"] = k.to(torch.bfloat16)
+    q, kk, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, kk, v, causal=causal)
+    assert eta.get_error() == 0
+    Or, Lr = oracle.attention(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                              causal=causal)
+    assert np.abs(Lr[0, 0, 200:] - Lr[0, 0, 200:].min()).max() > 90  # the jump is really there
+    check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what="max jump")
+
+
 def test_k_outliers():
     run(1, 4, 1, 512, 512, 128, True, seed=12, k_outlier=0.01)
 
