@@ -16,8 +16,9 @@
 // 128 x 128 tile.
 //
 // GB300 mapping, one CTA = two 128-row Q tiles of one (batch, query head):
-//   warp 8      TMA producer: Q once, then K_j / V_j into 2-stage rings
-//               (cp.async.bulk.tensor, 128-byte swizzle, mbarrier tx counts);
+//   warp 8      TMA producers (cp.async.bulk.tensor, 128-byte swizzle,
+//               mbarrier tx counts): lane 0 loads Q once and streams K_j
+//               into a 2-stage ring, lane 1 streams V_j into a 3-stage ring;
 //   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T with tcgen05.mma
 //               (both operands in shared memory, fp32 accumulator in TMEM),
 //               then O_i += P_i V_j with P_i read from TMEM.  Issue order
@@ -25,6 +26,7 @@
 //               softmax runs, the tensor core works on the other tile;
 //   warps 0-3   softmax of Q tile 0, one thread per query row (TMEM lane);
 //   warps 4-7   softmax of Q tile 1.
+// The softmax uses the packed fp32x2 FMA/ADD and three-input max of sm_100+.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it.
 // P_i overwrites the first columns of S_i.  The running max only moves when
 // the new maximum exceeds it by more than a threshold (log2 units), so O is
@@ -48,16 +50,18 @@ namespace fwd {
 constexpr int BM = 128;          // query rows per Q tile
 constexpr int BN = 128;          // keys per K/V tile
 constexpr int NQT = 2;           // Q tiles per CTA
-constexpr int NSTAGE = 2;        // K and V ring depth
+constexpr int NSK = 2;           // K ring depth
+constexpr int NSV = 3;           // V ring depth
 constexpr int HALF = 128 * 128;  // 128 rows x 128 bytes: one 128-byte-swizzled slab of a tile
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int THREADS = 10 * 32;
+
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Bf16 {
   static constexpr bool kFp8 = false;
-  static constexpr int kElem = 1 * 2;  // bytes per element
-  static constexpr int kMmaK = 16;     // K elements per MMA instruction (32 bytes)
+  static constexpr int kElem = 2;        // bytes per element
+  static constexpr int kMmaK = 16;       // K elements per MMA instruction (32 bytes)
   static constexpr float kThresh = 8.f;  // lazy-rescale threshold, log2 units
   static constexpr float kPre = 0.f;     // log2 of the probability pre-scale
   static constexpr uint32_t kTypeBits = (1u << 7) | (1u << 10);  // A and B bf16
@@ -78,9 +82,9 @@ struct Cfg {
   static constexpr int TILE = NH * HALF;         // one 128 x D tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQT * TILE;
-  static constexpr int OFF_V = OFF_K + NSTAGE * TILE;
-  static constexpr int OFF_BAR = OFF_V + NSTAGE * TILE;
-  static constexpr int NBAR = 1 + 4 * NSTAGE + 3 * NQT + 1;
+  static constexpr int OFF_V = OFF_K + NSK * TILE;
+  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQT + 1;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
   static constexpr int P_REGS = BN * T::kElem / 4;  // 32-bit TMEM columns holding one P row
@@ -127,9 +131,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *k_full = bars + 1, *k_empty = k_full + NSTAGE;
-  uint64_t *v_full = k_empty + NSTAGE, *v_empty = v_full + NSTAGE;
-  uint64_t *s_full = v_empty + NSTAGE, *p_full = s_full + NQT, *o_full = p_full + NQT;
+  uint64_t *k_full = bars + 1, *k_empty = k_full + NSK;
+  uint64_t *v_full = k_empty + NSK, *v_empty = v_full + NSV;
+  uint64_t *s_full = v_empty + NSV, *p_full = s_full + NQT, *o_full = p_full + NQT;
   uint64_t *done_bar = o_full + NQT;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
@@ -170,9 +174,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -190,11 +196,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_ptr;
 
   if (warp == WARP_TMA) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ producers
+    const int zk = b * p.Hkv + hkv;
+    if (lane == 0) {  // Q, then the K ring
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
       mbar_arrive_expect_tx(q_full, NQT * C::TILE);
 #pragma unroll
       for (int i = 0; i < NQT; ++i)
@@ -202,19 +208,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int h = 0; h < C::NH; ++h)
           tma_load_3d(smem + C::OFF_Q + i * C::TILE + h * HALF, &tmq, q_full, h * (128 / T::kElem), q0 + i * BM,
                       bh);
-      const int zk = b * p.Hkv + hkv;
-      int nk = 0, nv = 0;
+      int nk = 0;
       for (int j = 0; j < nkv; ++j) {
-        const int slot = j % NSTAGE;
-        const uint32_t par = ((j / NSTAGE) - 1) & 1;
-        if (j >= NSTAGE && !mbar_wait(&k_empty[slot], par, p.timeout_ns, p.err)) break;
+        const int slot = j % NSK;
+        if (j >= NSK && !mbar_wait(&k_empty[slot], ((j / NSK) - 1) & 1, p.timeout_ns, p.err)) break;
         mbar_arrive_expect_tx(&k_full[slot], C::TILE);
 #pragma unroll
         for (int h = 0; h < C::NH; ++h)
           tma_load_3d(smem + C::OFF_K + slot * C::TILE + h * HALF, &tmk, &k_full[slot], h * (128 / T::kElem),
                       j * BN, zk);
         nk = j + 1;
-        if (j >= NSTAGE && !mbar_wait(&v_empty[slot], par, p.timeout_ns, p.err)) break;
+      }
+      // Leave only once every copy issued here has landed.
+      mbar_wait(q_full, 0, p.timeout_ns, p.err);
+      for (int t = max(0, nk - NSK); t < nk; ++t) mbar_wait(&k_full[t % NSK], (t / NSK) & 1, p.timeout_ns, p.err);
+    } else if (lane == 1) {  // the V ring
+      tma_prefetch_desc(&tmv);
+      int nv = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int slot = j % NSV;
+        if (j >= NSV && !mbar_wait(&v_empty[slot], ((j / NSV) - 1) & 1, p.timeout_ns, p.err)) break;
         mbar_arrive_expect_tx(&v_full[slot], C::TILE);
 #pragma unroll
         for (int h = 0; h < C::NH; ++h)
@@ -222,20 +235,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                       j * BN, zk);
         nv = j + 1;
       }
-      // Leave only once every copy issued here has landed.
-      mbar_wait(q_full, 0, p.timeout_ns, p.err);
-      for (int t = max(0, nk - NSTAGE); t < nk; ++t)
-        mbar_wait(&k_full[t % NSTAGE], (t / NSTAGE) & 1, p.timeout_ns, p.err);
-      for (int t = max(0, nv - NSTAGE); t < nv; ++t)
-        mbar_wait(&v_full[t % NSTAGE], (t / NSTAGE) & 1, p.timeout_ns, p.err);
+      for (int t = max(0, nv - NSV); t < nv; ++t) mbar_wait(&v_full[t % NSV], (t / NSV) & 1, p.timeout_ns, p.err);
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issue
+    // One thread issues both Q tiles' chains in the order
+    // P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): while one tile's softmax runs the
+    // tensor core works on the other tile, and each group of MMAs runs
+    // contiguously so its result is ready as early as possible.
     if (lane == 0) {
       const uint32_t qs = smem_u32(smem + C::OFF_Q), ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V);
       // S_i = Q_i K_j^T: K-major operands, 32 bytes of the head dimension per instruction
       auto issue_s = [&](int i, int j) {
-        const int slot = j % NSTAGE;
+        const int slot = j % NSK;
 #pragma unroll
         for (int kk = 0; kk < D / T::kMmaK; ++kk) {
           const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto issue_pv = [&](int i, int j) -> bool {
         if (!mbar_wait(&p_full[i], j & 1, p.timeout_ns, p.err)) return false;
         tc_fence_after();
-        const int slot = j % NSTAGE;
+        const int slot = j % NSV;
 #pragma unroll
         for (int kk = 0; kk < BN / T::kMmaK; ++kk)
           mma_pv<T>(tmem + C::col_o(i), tmem + C::col_s(i) + kk * 8,
@@ -267,21 +279,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < nkv; ++j) {
-        const int slot = j % NSTAGE;
         const bool next = j + 1 < nkv;
-        if (!mbar_wait(&v_full[slot], (j / NSTAGE) & 1, p.timeout_ns, p.err)) break;
+        if (!mbar_wait(&v_full[j % NSV], (j / NSV) & 1, p.timeout_ns, p.err)) break;
         tc_fence_after();
         if (j < nkv_t[0] && !issue_pv(0, j)) break;
         if (next) {
-          if (!mbar_wait(&k_full[(j + 1) % NSTAGE], ((j + 1) / NSTAGE) & 1, p.timeout_ns, p.err)) break;
+          if (!mbar_wait(&k_full[(j + 1) % NSK], ((j + 1) / NSK) & 1, p.timeout_ns, p.err)) break;
           tc_fence_after();
           if (j + 1 < nkv_t[0]) issue_s(0, j + 1);
         }
         if (j < nkv_t[1] && !issue_pv(1, j)) break;
-        tc_commit(&v_empty[slot]);
+        tc_commit(&v_empty[j % NSV]);
         if (next) {
           if (j + 1 < nkv_t[1]) issue_s(1, j + 1);
-          tc_commit(&k_empty[(j + 1) % NSTAGE]);
+          tc_commit(&k_empty[(j + 1) % NSK]);
         }
       }
       tc_commit(done_bar);
@@ -324,20 +335,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t s[128];
       tmem_ld128(taddr + s_col, s);
       const int kb = j * BN;
-      if (kb + BN - 1 > lim) {  // diagonal or ragged tile: mask keys past lim
+      const bool masked = kb + BN - 1 > lim;  // diagonal or ragged tile
+      if (masked) {
 #pragma unroll
         for (int e = 0; e < 128; ++e)
           if (kb + e > lim) s[e] = __float_as_uint(-CUDART_INF_F);
       }
-      float mx8[8];
+      float mx4[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+      for (int u = 0; u < 4; ++u) mx4[u] = __uint_as_float(s[u]);
 #pragma unroll
-      for (int e = 8; e < 128; e += 8)
+      for (int e = 4; e < 128; e += 8)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[e + u]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int u = 0; u < 4; ++u)
+          mx4[u] = fmax3(mx4[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 4 + u]));
+      const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
       const float m_new = fmaxf(m_use, mx * cj);
       float alpha = 1.f;
       const bool moved = m_new > m_use + T::kThresh;  // also true on the first finite max
@@ -350,33 +362,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         m_use = m_new;
       }
       const float bias = e_off - ((m_use == -CUDART_INF_F) ? 0.f : m_use);
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t c2 = f2_pack(cj, cj), b2 = f2_pack(bias, bias);
+      uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
       uint32_t pk[C::P_REGS];
-      if constexpr (T::kFp8) {
 #pragma unroll
-        for (int e = 0; e < 128; e += 4) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[e]), cj, bias));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cj, bias));
-          const float p2 = fast_exp2(fmaf(__uint_as_float(s[e + 2]), cj, bias));
-          const float p3 = fast_exp2(fmaf(__uint_as_float(s[e + 3]), cj, bias));
-          rs4[0] += p0;
-          rs4[1] += p1;
-          rs4[2] += p2;
-          rs4[3] += p3;
-          const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p2, p3), __NV_SATFINITE, __NV_E4M3);
-          pk[e / 4] = lo | (hi << 16);
+      for (int e = 0; e < 128; e += 8) {
+        float pr[8];
+#pragma unroll
+        for (int u = 0; u < 8; u += 2) {
+          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1])), c2, b2);
+          f2_unpack(x2, pr[u], pr[u + 1]);
         }
-      } else {
 #pragma unroll
-        for (int e = 0; e < 128; e += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[e]), cj, bias));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[e + 1]), cj, bias));
-          rs4[(e >> 1) & 3] += p0 + p1;
-          pk[e / 2] = pack_bf16x2(p0, p1);
+        for (int u = 0; u < 8; ++u) pr[u] = fast_exp2(pr[u]);
+        acc2[0] = f2_add(acc2[0], f2_add(f2_pack(pr[0], pr[1]), f2_pack(pr[2], pr[3])));
+        acc2[1] = f2_add(acc2[1], f2_add(f2_pack(pr[4], pr[5]), f2_pack(pr[6], pr[7])));
+        if constexpr (T::kFp8) {
+#pragma unroll
+          for (int u = 0; u < 8; u += 4) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(pr[u], pr[u + 1]), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi =
+                __nv_cvt_float2_to_fp8x2(make_float2(pr[u + 2], pr[u + 3]), __NV_SATFINITE, __NV_E4M3);
+            pk[(e + u) / 4] = lo | (hi << 16);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) pk[(e + u) / 2] = pack_bf16x2(pr[u], pr[u + 1]);
         }
       }
-      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      float r0, r1, r2, r3;
+      f2_unpack(acc2[0], r0, r1);
+      f2_unpack(acc2[1], r2, r3);
+      const float rs = (r0 + r1) + (r2 + r3);
       l = l * alpha + (T::kFp8 ? rs * fast_exp2(-e_off) : rs);
 #pragma unroll
       for (int c = 0; c < C::P_REGS / 32; ++c) {
