@@ -85,6 +85,11 @@ def max_over_ranks(x: float, ws: int) -> float:
     return float(t.item())
 
 
+def whole_job_tflops(flops_per_step: float, world_size: int, step_ms_max: float) -> float:
+    """Work of all replicas over the slowest rank's step time, in TFLOP/s."""
+    return flops_per_step * world_size / (step_ms_max * 1e-3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -206,16 +211,16 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
     flops = acc.prefill_flops(B, Hq, S, S, D, causal)
     ms = statistics.mean(ts)
     ach = flops / (ms * 1e-3) / 1e12
-    digest = source_digest("fwd_bf16.cu", "ptx.cuh")
+    digest = source_digest("fwd_kernel.cuh", "fwd_bf16.cu", "ptx.cuh")
     res = {
         "metric": "attention TFLOP/s (bf16 prefill)", "unit": "TFLOP/s", "value": ach,
         "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Sk": S, "D": D, "causal": causal},
         "flops_per_step": flops,
-        "roofline": {"bound": "tensor", "kernel": "fwd_bf16_kernel", "achieved": ach, "peak": peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Bf16,128>", "achieved": ach, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
                      "peak_source": peaks["source"] + " bf16 burst",
-                     "traffic": dram_traffic("fwd_bf16_kernel", name, digest),
+                     "traffic": dram_traffic("fwd_kernel<Bf16,128>", name, digest),
                      "algorithmic_bytes": acc.prefill_bytes(B, Hq, Hkv, S, S, D)},
         "gpu_launches": len(ts),
     }
@@ -296,15 +301,15 @@ def run_fp8(steps, warmup, flush, peaks):
     ms = statistics.mean(ts)
     ach = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-    digest = source_digest("fwd_fp8.cu", "ptx.cuh")
+    digest = source_digest("fwd_kernel.cuh", "fwd_fp8.cu", "ptx.cuh")
     return {
         "metric": "attention TFLOP/s (FP8 e4m3 prefill)", "unit": "TFLOP/s", "value": ach,
         "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Sk": S, "D": D, "causal": causal},
-        "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": ach, "peak": peak,
+        "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Fp8,128>", "achieved": ach, "peak": peak,
                      "unit": "TFLOP/s", "frac": ach / peak,
                      "peak_source": peaks["source"] + " bf16 burst x 2 (nominal FP8/BF16 ratio)",
-                     "traffic": dram_traffic("fwd_fp8_kernel", name, digest),
+                     "traffic": dram_traffic("fwd_kernel<Fp8,128>", name, digest),
                      "algorithmic_bytes": acc.prefill_bytes(B, Hq, Hkv, S, S, D, elem_bytes=1)
                      + acc.fp8_scale_bytes(B, Hq, Hkv, S, S, D)},
         "gpu_launches": len(ts),
@@ -407,7 +412,7 @@ def main():
     clk = clocks.stop()
     if rank != 0:
         return
-    value = head["flops_per_step"] * ws / (step_ms * 1e-3) / 1e12
+    value = whole_job_tflops(head["flops_per_step"], ws, step_ms)
     line = {
         "metric": "attention TFLOP/s (prefill) & KV-read GB/s (decode), 1xGB300, % of roofline",
         "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
