@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--only", choices=["train_prefill_mha", "long_gqa_prefill", "gqa_decode", "fp8_prefill"],
+                    help="run one workload leg alone and print its figures (for profiling)")
     return ap.parse_args()
 
 
@@ -389,6 +391,16 @@ def main():
     import torch
     peaks = load_peaks()
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > 129 MB L2
+    if args.only:
+        if args.only == "gqa_decode":
+            res = run_decode(args.steps, args.warmup, flush, peaks)
+        elif args.only == "fp8_prefill":
+            res = run_fp8(args.steps, args.warmup, flush, peaks)
+        else:
+            res = run_prefill(args.only, args.steps, args.warmup, flush, peaks)
+        if rank == 0:
+            print(json.dumps(dict(res, only=args.only)), flush=True)
+        return
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
