@@ -19,7 +19,9 @@
 //     log2-LSE go to the workspace.
 // Kernel 2 (decode_combine_kernel) merges the splits of each (sequence, head)
 // with log-sum-exp weights -- the same running max / running sum update
-// ("Hardware Co-Design", FlashAttention section) applied to whole splits.
+// ("Hardware Co-Design", FlashAttention section) applied to whole splits.  It
+// is launched as a programmatic dependent of kernel 1, so it is resident and
+// waiting when the last splits finish instead of paying a launch gap.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -80,6 +82,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int split = blockIdx.x;
   const int kvh = blockIdx.y / p.nhc, hc = blockIdx.y % p.nhc;
   const int b = blockIdx.z;
+  // The merge kernel may be scheduled as soon as every CTA of this grid has
+  // started; it waits for this grid's results before reading them.
+  griddep_launch_dependents();
   const int L = max(0, min(p.seqlens[b], p.Lmax));
   const int s0 = split * p.chunk;
   if (s0 >= L) return;  // the whole CTA leaves together, before any barrier
@@ -313,6 +318,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(CombineParams p) {
   const int bh = blockIdx.x;
   const int b = bh / p.Hq;
   const int d = threadIdx.x;
+  griddep_wait();  // launched early (programmatic dependent launch): wait for the splits
   const int L = max(0, min(p.seqlens[b], p.Lmax));
   const int ns = (L + p.chunk - 1) / p.chunk;
   if (ns == 0) {  // empty sequence
@@ -373,8 +379,17 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   c.Lmax = a.Lmax;
   c.chunk = a.chunk;
   c.nsplit = a.nsplit;
-  decode_combine_kernel<D><<<a.B * a.Hq, D, 0, st>>>(c);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.Hq);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, c);
 }
 
 }  // namespace dec
