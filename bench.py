@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--only", choices=["train_prefill_mha", "long_gqa_prefill", "gqa_decode", "fp8_prefill"],
+    ap.add_argument("--only", choices=["train_prefill_mha", "long_gqa_prefill", "gqa_decode", "gqa_decode_paged",
+                                       "fp8_prefill"],
                     help="run one workload leg alone and print its figures (for profiling)")
     return ap.parse_args()
 
@@ -284,6 +285,45 @@ def run_decode(steps, warmup, flush, peaks):
     }
 
 
+def run_decode_paged(steps, warmup, flush, peaks):
+    import torch
+    import exact_tiled_attention_15_gb300 as eta
+    from exact_tiled_attention_15_gb300 import accounting as acc, workloads
+    name = "gqa_decode_paged"
+    cfg = workloads.WORKLOADS[name]
+    B, Hq, Hkv, D, ps = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["page_size"]
+    w = workloads.make_paged_decode(B, Hq, Hkv, D, cfg["Lmin"], cfg["Lmax"], ps, seed=0, poison=False)
+    dev = torch.device("cuda")
+    t = {n: w[n].to(dev) for n in ("q", "k_pages", "v_pages", "block_table", "seqlens")}
+    del w["kcache"], w["vcache"]
+    ws = torch.empty(eta.decode_workspace_bytes(B, Hq, Hkv, t["block_table"].shape[1] * ps, D), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(t["q"])
+    lse = torch.empty(B, Hq, device=dev, dtype=torch.float32)
+    fn = lambda: eta.decode_paged(t["q"], t["k_pages"], t["v_pages"], t["block_table"], t["seqlens"],  # noqa: E731
+                                  workspace=ws, out=o, lse_out=lse)
+    ts = time_steps(fn, steps, warmup, flush)
+    if eta.get_error() != 0:
+        raise RuntimeError("paged decode: device-side error")
+    seqlens = w["seqlens"].tolist()
+    nbytes = acc.decode_bytes(seqlens, B, Hq, Hkv, D) + 4 * sum(-(-x // ps) for x in seqlens)
+    ms = statistics.mean(ts)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    digest = source_digest("decode.cu", "ptx.cuh")
+    return {
+        "metric": "KV-read GB/s (bf16 GQA decode, paged KV cache)", "unit": "GB/s", "value": gbs,
+        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Lmin": cfg["Lmin"],
+                   "Lmax": cfg["Lmax"], "page_size": ps, "sum_seqlens": int(sum(seqlens))},
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,paged>+decode_combine_kernel",
+                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"] + " HBM copy",
+                     "traffic": dram_traffic("decode_split_kernel<128,paged>", name, digest),
+                     "algorithmic_bytes": nbytes},
+        "gpu_launches": 2 * len(ts),
+    }
+
+
 def run_fp8(steps, warmup, flush, peaks):
     import torch
     import exact_tiled_attention_15_gb300 as eta
@@ -394,6 +434,8 @@ def main():
     if args.only:
         if args.only == "gqa_decode":
             res = run_decode(args.steps, args.warmup, flush, peaks)
+        elif args.only == "gqa_decode_paged":
+            res = run_decode_paged(args.steps, args.warmup, flush, peaks)
         elif args.only == "fp8_prefill":
             res = run_fp8(args.steps, args.warmup, flush, peaks)
         else:
@@ -416,6 +458,7 @@ def main():
     if not args.no_extras:
         extras["long_gqa_prefill"] = run_prefill("long_gqa_prefill", max(5, args.steps // 4), args.warmup, flush, peaks)
         extras["gqa_decode"] = run_decode(args.steps, args.warmup, flush, peaks)
+        extras["gqa_decode_paged"] = run_decode_paged(args.steps, args.warmup, flush, peaks)
         try:
             extras["fp8_prefill"] = run_fp8(args.steps, args.warmup, flush, peaks)
         except Exception as e:  # reported, not hidden

@@ -26,6 +26,7 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_get_error": (_I, [_P]),
@@ -136,6 +137,37 @@ def decode(q, kcache, vcache, seqlens, scale=None, workspace=None, return_lse=Tr
                            B, Hq, Hkv, Lmax, D, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(q.device))
     _check(st, "attn_decode")
+    return o, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, scale=None, workspace=None, return_lse=True,
+                 out=None, lse_out=None):
+    """Decode against a paged cache: pools [num_pages, Hkv, page_size, D] bf16,
+    block_table [B, max_blocks] int32 -> (o, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    B, Hq, D = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_blocks = block_table.shape[1]
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or k_pages.shape[3] != D:
+        raise ValueError("k_pages and v_pages must be [num_pages, Hkv, page_size, D] matching q")
+    if block_table.shape[0] != B or seqlens.shape[0] != B:
+        raise ValueError("block_table and seqlens must have B rows")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    nbytes = decode_workspace_bytes(B, Hq, Hkv, max_blocks * page_size, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    o = out if out is not None else torch.empty_like(q)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), _ptr(o),
+                                 _ptr(lse), B, Hq, Hkv, page_size, max_blocks, num_pages, D, scale, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(q.device))
+    _check(st, "attn_decode_paged")
     return o, lse
 
 

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -177,6 +178,59 @@ attn_status attn_decode(const void *q, const void *kcache, const void *vcache, c
   attn::DecodeArgs a{};
   a.q = q;
   a.seqlens = seqlens;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.D = D;
+  a.chunk = attn::decode_chunk(B, Hq, Hkv, Lmax);
+  a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
+  a.scale = scale;
+  a.timeout_ns = kDefaultTimeoutNs;
+  a.err = error_word();
+  if (!a.err) return ATTN_ERR_CUDA;
+  const size_t rows = (size_t)B * Hq * a.nsplit;
+  size_t o_bytes = (rows * (size_t)D * sizeof(float) + 255) / 256 * 256;
+  a.part_o = static_cast<float *>(workspace);
+  a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+  return from_cuda(attn::launch_decode(a, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table,
+                              const int32_t *seqlens, void *o, float *lse, int B, int Hq, int Hkv, int page_size,
+                              int max_blocks, int num_pages, int D, float scale, void *workspace,
+                              size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seqlens || !o || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_pages < 1 || D < 1 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (page_size < 1 || (int64_t)max_blocks * page_size > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+  if (bad_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqlens) | reinterpret_cast<uintptr_t>(block_table)) & 3u) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID_ARG;
+  const int Lmax = max_blocks * page_size;
+  if (workspace_bytes < attn_decode_workspace_bytes(B, Hq, Hkv, Lmax, D)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128 && page_size != 256)
+    return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)num_pages * Hkv > (1LL << 30) || (int64_t)B * Hq > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
+  if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
+  const uint32_t box_rows = page_size < 64 ? (uint32_t)page_size : 64u;
+  CUtensorMap tk, tv;
+  if (!make_tmap(&tk, k_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, page_size, (uint64_t)num_pages * Hkv, 64,
+                 box_rows) ||
+      !make_tmap(&tv, v_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, page_size, (uint64_t)num_pages * Hkv, 64,
+                 box_rows))
+    return ATTN_ERR_CUDA;
+  attn::DecodeArgs a{};
+  a.q = q;
+  a.seqlens = seqlens;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.page_size = page_size;
   a.o = o;
   a.lse = lse;
   a.B = B;

@@ -54,6 +54,8 @@ struct Cfg {
 struct Params {
   const __nv_bfloat16 *q;
   const int32_t *seqlens;
+  const int32_t *block_table;  // paged cache only: [B, max_blocks]
+  int max_blocks, page_size, box_rows;
   float *part_o;
   float *part_lse;
   int B, Hq, Hkv, Lmax, chunk, nsplit, g, nhc;
@@ -68,7 +70,11 @@ __device__ __forceinline__ uint32_t tile_off(int row, int c) {
   return (c >> 3) * HALF_BYTES + row * 128 + (((c & 7) ^ (row & 7)) << 4);
 }
 
-template <int D>
+// PAGED: K/V live in a page pool [num_pages, Hkv, page_size, D]; position t
+// of sequence b is row t % page_size of page block_table[b, t / page_size]
+// ("Fast Inference and Training at Scale" §6.3, PagedAttention).  Each 64-key
+// stage is then gathered by boxes of min(page_size, 64) rows.
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(THREADS, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Params p) {
   using C = Cfg<D>;
@@ -106,28 +112,73 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
 
   if (warp == NCW) {  // ---------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-      const int z = b * p.Hkv + kvh;
+    if constexpr (!PAGED) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        const int z = b * p.Hkv + kvh;
+        int issued = 0;
+        for (int t = 0; t < nst; ++t) {
+          const int slot = t % NST;
+          if (t >= NST && !mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.timeout_ns, p.err)) break;
+          uint8_t *kt = smem + slot * C::STAGE_BYTES;
+          uint8_t *vt = kt + C::TILE_BYTES;
+          mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
+          const int y = s0 + t * KS;
+#pragma unroll
+          for (int hf = 0; hf < C::NHALF; ++hf) {
+            tma_load_3d(kt + hf * HALF_BYTES, &tmk, &full[slot], hf * 64, y, z);
+            tma_load_3d(vt + hf * HALF_BYTES, &tmv, &full[slot], hf * 64, y, z);
+          }
+          issued = t + 1;
+        }
+        // Do not leave while a copy this thread issued may still be landing.
+        for (int t = max(0, issued - NST); t < issued; ++t)
+          mbar_wait(&full[t % NST], (t / NST) & 1, p.timeout_ns, p.err);
+      }
+    } else {
+      // The whole warp walks the block table, 32 entries per coalesced load;
+      // lane 0 issues the copies.
+      if (lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+      }
+      const int32_t *table = p.block_table + (size_t)b * p.max_blocks;
+      int win = -1, entry = 0;  // entries win .. win+31 of the table, one per lane
       int issued = 0;
       for (int t = 0; t < nst; ++t) {
         const int slot = t % NST;
-        if (t >= NST && !mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.timeout_ns, p.err)) break;
+        if (t >= NST && !__all_sync(0xffffffffu, mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.timeout_ns, p.err)))
+          break;
         uint8_t *kt = smem + slot * C::STAGE_BYTES;
         uint8_t *vt = kt + C::TILE_BYTES;
-        mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
         const int y = s0 + t * KS;
+        for (int r = 0; r < KS; r += p.box_rows) {
+          const int pos = y + r;
+          int page = 0;  // rows past the sequence's end come from page 0 and are masked
+          if (pos < L) {
+            const int blk = pos / p.page_size;
+            if (win < 0 || blk >= win + 32) {
+              win = blk;
+              entry = (blk + lane < p.max_blocks) ? __ldg(&table[blk + lane]) : 0;
+            }
+            page = __shfl_sync(0xffffffffu, entry, blk - win);
+          }
+          if (lane == 0) {
+            const int z = page * p.Hkv + kvh, off = pos % p.page_size;
 #pragma unroll
-        for (int hf = 0; hf < C::NHALF; ++hf) {
-          tma_load_3d(kt + hf * HALF_BYTES, &tmk, &full[slot], hf * 64, y, z);
-          tma_load_3d(vt + hf * HALF_BYTES, &tmv, &full[slot], hf * 64, y, z);
+            for (int hf = 0; hf < C::NHALF; ++hf) {
+              tma_load_3d(kt + hf * HALF_BYTES + r * 128, &tmk, &full[slot], hf * 64, off, z);
+              tma_load_3d(vt + hf * HALF_BYTES + r * 128, &tmv, &full[slot], hf * 64, off, z);
+            }
+          }
         }
         issued = t + 1;
       }
-      // Do not leave while a copy this thread issued may still be landing.
-      for (int t = max(0, issued - NST); t < issued; ++t)
-        mbar_wait(&full[t % NST], (t / NST) & 1, p.timeout_ns, p.err);
+      if (lane == 0)
+        for (int t = max(0, issued - NST); t < issued; ++t)
+          mbar_wait(&full[t % NST], (t / NST) & 1, p.timeout_ns, p.err);
     }
     return;
   }
@@ -340,7 +391,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(CombineParams p) {
   if (d == 0 && p.lse) p.lse[bh] = (M + log2f(tot)) * 0.69314718055994530942f;
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv, cudaStream_t st) {
   using C = Cfg<D>;
   const int g = a.Hq / a.Hkv;
@@ -348,6 +399,10 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   Params p;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.seqlens = a.seqlens;
+  p.block_table = a.block_table;
+  p.max_blocks = a.max_blocks;
+  p.page_size = a.page_size;
+  p.box_rows = a.page_size < KS ? a.page_size : KS;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
   p.B = a.B;
@@ -361,12 +416,12 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
   p.err = a.err;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (a.B > 65535 || (long)a.Hkv * nhc > 65535) return cudaErrorNotSupported;
   dim3 grid(a.nsplit, a.Hkv * nhc, a.B);
-  decode_split_kernel<D><<<grid, THREADS, C::SMEM_BYTES, st>>>(tmk, tmv, p);
+  decode_split_kernel<D, PAGED><<<grid, THREADS, C::SMEM_BYTES, st>>>(tmk, tmv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CombineParams c;
@@ -407,8 +462,11 @@ int decode_chunk(int B, int Hq, int Hkv, int Lmax) {
 
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           cudaStream_t stream) {
-  if (a.D == 128) return dec::launch<128>(a, tmap_k, tmap_v, stream);
-  if (a.D == 64) return dec::launch<64>(a, tmap_k, tmap_v, stream);
+  const bool paged = a.block_table != nullptr;
+  if (a.D == 128) return paged ? dec::launch<128, true>(a, tmap_k, tmap_v, stream)
+                               : dec::launch<128, false>(a, tmap_k, tmap_v, stream);
+  if (a.D == 64) return paged ? dec::launch<64, true>(a, tmap_k, tmap_v, stream)
+                              : dec::launch<64, false>(a, tmap_k, tmap_v, stream);
   return cudaErrorInvalidValue;
 }
 

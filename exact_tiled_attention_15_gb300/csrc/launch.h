@@ -16,6 +16,8 @@ inline int decode_nsplit(int Lmax, int chunk) { return (Lmax + chunk - 1) / chun
 struct DecodeArgs {
   const void *q;
   const int32_t *seqlens;
+  const int32_t *block_table;  // nullptr: contiguous cache; else [B, max_blocks] page ids
+  int max_blocks, page_size;
   void *o;
   float *lse;
   float *part_o;    // [B, Hq, nsplit, D]
@@ -27,7 +29,9 @@ struct DecodeArgs {
 };
 
 // Launch split kernel + combine kernel.  tmap_k / tmap_v describe the caches as
-// 3-D tensors (D, Lmax, B*Hkv) with 64 x 64 boxes and 128-byte swizzle.
+// 3-D tensors (D, Lmax, B*Hkv) with 64 x 64 boxes and 128-byte swizzle, or for a
+// paged cache the pools as (D, page_size, num_pages*Hkv) with 64 x
+// min(page_size, 64) boxes.
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           cudaStream_t stream);
 

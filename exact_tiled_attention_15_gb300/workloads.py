@@ -33,6 +33,7 @@ WORKLOADS = {
     "long_gqa_prefill": dict(kind="prefill", B=1, Hq=32, Hkv=8, S=16384, D=128, causal=True,
                              k_outlier_frac=0.01, k_outlier_mult=20.0),
     "gqa_decode": dict(kind="decode", B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192),
+    "gqa_decode_paged": dict(kind="paged_decode", B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192, page_size=64),
     "fp8_prefill": dict(kind="fp8", B=2, Hq=16, Hkv=16, S=8192, D=128, causal=False,
                         outlier_frac=0.005, outlier_mult=50.0),
 }
@@ -90,6 +91,40 @@ def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True, seqlens=Non
             off += n
         caches.append(c)
     return dict(q=to_bf16(q), kcache=caches[0], vcache=caches[1], seqlens=torch.from_numpy(seqlens))
+
+
+def make_paged_decode(B, Hq, Hkv, D, Lmin, Lmax, page_size, seed=0, poison=True, seqlens=None, spare_pages=3):
+    """The decode workload of make_decode, stored in a paged KV cache.
+
+    K and V rows of sequence b, position t live in page block_table[b, t //
+    page_size] at row t % page_size of a shared pool [num_pages, Hkv,
+    page_size, D].  Pages are handed out in a seeded random order; unused
+    rows (and table entries past a sequence's last page, which point at
+    page 0) hold NaN when ``poison``.  Returns q, k_pages, v_pages,
+    block_table [B, ceil(Lmax / page_size)] int32, seqlens, and the
+    contiguous kcache/vcache the pages were filled from.
+    """
+    w = make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=seed, poison_tail=poison, seqlens=seqlens)
+    sl = w["seqlens"].numpy()
+    max_blocks = -(-Lmax // page_size)
+    need = [-(-int(n) // page_size) for n in sl]
+    num_pages = sum(need) + spare_pages
+    order = np.random.default_rng(seed + 1).permutation(num_pages)
+    fill = float("nan") if poison else 0.0
+    kp = torch.full((num_pages, Hkv, page_size, D), fill, dtype=torch.bfloat16)
+    vp = torch.full((num_pages, Hkv, page_size, D), fill, dtype=torch.bfloat16)
+    table = np.zeros((B, max_blocks), dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        for blk in range(need[b]):
+            pid = int(order[nxt])
+            nxt += 1
+            table[b, blk] = pid
+            r0, r1 = blk * page_size, min(int(sl[b]), (blk + 1) * page_size)
+            kp[pid, :, :r1 - r0] = w["kcache"][b, :, r0:r1]
+            vp[pid, :, :r1 - r0] = w["vcache"][b, :, r0:r1]
+    return dict(q=w["q"], k_pages=kp, v_pages=vp, block_table=torch.from_numpy(table), seqlens=w["seqlens"],
+                kcache=w["kcache"], vcache=w["vcache"], page_size=page_size)
 
 
 def hadamard(n: int) -> np.ndarray:

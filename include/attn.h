@@ -98,6 +98,27 @@ attn_status attn_decode(const void *q, const void *kcache, const void *vcache,
                         int B, int Hq, int Hkv, int Lmax, int D, float scale,
                         void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
+/*
+ * attn_decode_paged -- attn_decode against a paged KV cache ("Fast Inference
+ * and Training at Scale" §6.3, PagedAttention: the cache lives in fixed-size
+ * blocks reached through a per-sequence block table).
+ *   k_pages, v_pages [num_pages, Hkv, page_size, D] bf16: the shared page pool.
+ *   block_table [B, max_blocks] int32: position t of sequence b is row
+ *           t % page_size of page block_table[b, t / page_size].  Only the
+ *           entries covering positions < seqlens[b] are read; an entry
+ *           outside [0, num_pages) reads zeros (no fault) and gives a wrong
+ *           but finite result for that sequence.
+ *   seqlens [B] int32, 0 <= seqlens[b] <= max_blocks * page_size.
+ *   page_size in {16, 32, 64, 128, 256} else ATTN_ERR_UNSUPPORTED.
+ *   workspace: at least attn_decode_workspace_bytes(B, Hq, Hkv,
+ *           max_blocks * page_size, D) bytes, 256-byte aligned.
+ *   q, o, lse, D, scale and errors as for attn_decode.
+ */
+attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                              const int32_t *block_table, const int32_t *seqlens, void *o, float *lse,
+                              int B, int Hq, int Hkv, int page_size, int max_blocks, int num_pages, int D,
+                              float scale, void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
 /* Size of the fixed device scratch array used by attn_decode_noalloc. */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
 

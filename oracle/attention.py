@@ -142,3 +142,23 @@ def merge_partials(o_parts, lse_parts):
     lse = np.where(tot > 0, m_safe + np.log(tot_safe), -np.inf)
     O = (w[..., None] * o_parts).sum(axis=0) / tot_safe[..., None]
     return O, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, page_size: int, scale: float | None = None):
+    """Decode against a paged KV cache ("Fast Inference and Training at
+    Scale" §6.3, PagedAttention: a sequence's cache lives in fixed-size blocks
+    found through its block table).  Position t of sequence b is row
+    t % page_size of page block_table[b, t // page_size]; the rows are
+    gathered in position order and the result is `decode` on them.
+    """
+    B, Hq, D = np.asarray(q).shape
+    Hkv = k_pages.shape[1]
+    Lmax = block_table.shape[1] * page_size
+    kc = np.zeros((B, Hkv, Lmax, D))
+    vc = np.zeros((B, Hkv, Lmax, D))
+    for b in range(B):
+        for t in range(int(seqlens[b])):
+            page = int(block_table[b, t // page_size])
+            kc[b, :, t] = np.asarray(k_pages[page, :, t % page_size], dtype=np.float64)
+            vc[b, :, t] = np.asarray(v_pages[page, :, t % page_size], dtype=np.float64)
+    return decode(q, kc, vc, seqlens, scale)

@@ -116,3 +116,18 @@ def test_python_binding_rejects_cpu_tensors(lib):
         eta.fwd(q.float(), q, q)
     with pytest.raises(TypeError):
         eta.fwd("q", q, q)
+
+
+def test_decode_paged_validation(lib):
+    n = lib.attn_decode_workspace_bytes(4, 8, 2, 16 * 64, 128)
+
+    def dec(ps=64, table=A, mb=16, npages=40, wsb=n, D=128):
+        return lib.attn_decode_paged(p(A), p(A), p(A), p(table), p(A), p(A), None, 4, 8, 2, ps, mb, npages, D, 0.1,
+                                     p(A), wsb, None)
+
+    assert dec(table=0) == INVALID
+    assert dec(table=A + 2) == INVALID
+    assert dec(npages=0) == INVALID
+    assert dec(wsb=n - 1) == INVALID
+    assert dec(ps=48, mb=20, wsb=lib.attn_decode_workspace_bytes(4, 8, 2, 48 * 20, 128)) == UNSUPPORTED
+    assert dec(D=80, wsb=lib.attn_decode_workspace_bytes(4, 8, 2, 1024, 80)) == UNSUPPORTED
