@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--only", choices=["train_prefill_mha", "long_gqa_prefill", "gqa_decode", "gqa_decode_paged",
-                                       "fp8_prefill"],
+                                       "gqa_decode_T4", "fp8_prefill"],
                     help="run one workload leg alone and print its figures (for profiling)")
     return ap.parse_args()
 
@@ -324,6 +324,38 @@ def run_decode_paged(steps, warmup, flush, peaks):
     }
 
 
+def run_decode_multi(steps, warmup, flush, peaks, T=4):
+    import torch
+    import exact_tiled_attention_15_gb300 as eta
+    from exact_tiled_attention_15_gb300 import accounting as acc, workloads
+    name = "gqa_decode"
+    cfg = workloads.WORKLOADS[name]
+    B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
+    w = workloads.make_decode(B, Hq, Hkv, D, cfg["Lmin"], cfg["Lmax"], seed=0, poison_tail=False, T=T)
+    dev = torch.device("cuda")
+    q, kc, vc, sl = (w[n].to(dev) for n in ("q", "kcache", "vcache", "seqlens"))
+    ws = torch.empty(int(eta.lib().attn_decode_multi_workspace_bytes(B, Hq, Hkv, T, cfg["Lmax"], D)),
+                     dtype=torch.uint8, device=dev)
+    fn = lambda: eta.decode_multi(q, kc, vc, sl, causal=True, workspace=ws)  # noqa: E731
+    ts = time_steps(fn, steps, warmup, flush)
+    if eta.get_error() != 0:
+        raise RuntimeError("multi-token decode: device-side error")
+    seqlens = w["seqlens"].tolist()
+    nbytes = acc.decode_bytes(seqlens, B, Hq * T, Hkv, D)
+    ms = statistics.mean(ts)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": f"KV-read GB/s (bf16 GQA decode, {T} causal query tokens per sequence)", "unit": "GB/s",
+        "value": gbs, "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "config": {"workload": name + f"_T{T}", "B": B, "Hq": Hq, "Hkv": Hkv, "T": T, "D": D, "Lmin": cfg["Lmin"],
+                   "Lmax": cfg["Lmax"], "sum_seqlens": int(sum(seqlens))},
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel+decode_combine_kernel (T query tokens)",
+                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"] + " HBM copy", "traffic": None, "algorithmic_bytes": nbytes},
+        "gpu_launches": 2 * len(ts),
+    }
+
+
 def run_fp8(steps, warmup, flush, peaks):
     import torch
     import exact_tiled_attention_15_gb300 as eta
@@ -436,6 +468,8 @@ def main():
             res = run_decode(args.steps, args.warmup, flush, peaks)
         elif args.only == "gqa_decode_paged":
             res = run_decode_paged(args.steps, args.warmup, flush, peaks)
+        elif args.only == "gqa_decode_T4":
+            res = run_decode_multi(args.steps, args.warmup, flush, peaks, T=4)
         elif args.only == "fp8_prefill":
             res = run_fp8(args.steps, args.warmup, flush, peaks)
         else:
@@ -459,6 +493,7 @@ def main():
         extras["long_gqa_prefill"] = run_prefill("long_gqa_prefill", max(5, args.steps // 4), args.warmup, flush, peaks)
         extras["gqa_decode"] = run_decode(args.steps, args.warmup, flush, peaks)
         extras["gqa_decode_paged"] = run_decode_paged(args.steps, args.warmup, flush, peaks)
+        extras["gqa_decode_T4"] = run_decode_multi(args.steps, args.warmup, flush, peaks, T=4)
         try:
             extras["fp8_prefill"] = run_fp8(args.steps, args.warmup, flush, peaks)
         except Exception as e:  # reported, not hidden

@@ -5,9 +5,10 @@
 ``fwd``      bf16 prefill (causal or not, MHA/GQA/MQA) -> (O, LSE)
 ``decode``   one query token per sequence against a KV cache -> (O, LSE)
 ``decode_paged``  the same against a paged KV cache (block table) -> (O, LSE)
+``decode_multi``  T <= 16 query tokens per sequence (speculative verification) -> (O, LSE)
 ``fwd_fp8``  FP8 e4m3 prefill with one scale per 128x128 tile -> (O, LSE)
 
 All three call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import AttnError, decode, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, version  # noqa: F401
+from ._lib import AttnError, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, version  # noqa: F401

@@ -26,6 +26,8 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "attn_decode_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_decode_multi": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
@@ -137,6 +139,31 @@ def decode(q, kcache, vcache, seqlens, scale=None, workspace=None, return_lse=Tr
                            B, Hq, Hkv, Lmax, D, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(q.device))
     _check(st, "attn_decode")
+    return o, lse
+
+
+def decode_multi(q, kcache, vcache, seqlens, causal=True, scale=None, workspace=None, return_lse=True):
+    """T query tokens per sequence: q [B,Hq,T,D] against cache [B,Hkv,Lmax,D] -> (o [B,Hq,T,D], lse [B,Hq,T])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kcache, "kcache", torch.bfloat16, 4)
+    _need(vcache, "vcache", torch.bfloat16, 4)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    B, Hq, T, D = q.shape
+    Hkv, Lmax = kcache.shape[1], kcache.shape[2]
+    if tuple(vcache.shape) != tuple(kcache.shape) or kcache.shape[0] != B or kcache.shape[3] != D:
+        raise ValueError("kcache and vcache must be [B, Hkv, Lmax, D] matching q")
+    if seqlens.shape[0] != B:
+        raise ValueError("seqlens must have B entries")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    nbytes = int(lib().attn_decode_multi_workspace_bytes(B, Hq, Hkv, T, Lmax, D))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, T, device=q.device, dtype=torch.float32) if return_lse else None
+    st = lib().attn_decode_multi(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                 T, Lmax, D, 1 if causal else 0, scale, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(q.device))
+    _check(st, "attn_decode_multi")
     return o, lse
 
 

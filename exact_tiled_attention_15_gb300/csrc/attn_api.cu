@@ -148,10 +148,14 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || D < 1 || Hq % Hkv != 0) return 0;
-  const int chunk = attn::decode_chunk(B, Hq, Hkv, Lmax);
+  return attn_decode_multi_workspace_bytes(B, Hq, Hkv, 1, Lmax, D);
+}
+
+size_t attn_decode_multi_workspace_bytes(int B, int Hq, int Hkv, int T, int Lmax, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || T > 16 || Lmax < 1 || D < 1 || Hq % Hkv != 0) return 0;
+  const int chunk = attn::decode_chunk(B, Hq, Hkv, T, Lmax);
   const size_t ns = (size_t)attn::decode_nsplit(Lmax, chunk);
-  const size_t rows = (size_t)B * Hq * ns;
+  const size_t rows = (size_t)B * Hq * T * ns;
   size_t o_bytes = rows * (size_t)D * sizeof(float);
   o_bytes = (o_bytes + 255) / 256 * 256;
   return o_bytes + rows * sizeof(float);
@@ -185,7 +189,9 @@ attn_status attn_decode(const void *q, const void *kcache, const void *vcache, c
   a.Hkv = Hkv;
   a.Lmax = Lmax;
   a.D = D;
-  a.chunk = attn::decode_chunk(B, Hq, Hkv, Lmax);
+  a.T = 1;
+  a.causal = 0;
+  a.chunk = attn::decode_chunk(B, Hq, Hkv, 1, Lmax);
   a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
@@ -238,13 +244,59 @@ attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_
   a.Hkv = Hkv;
   a.Lmax = Lmax;
   a.D = D;
-  a.chunk = attn::decode_chunk(B, Hq, Hkv, Lmax);
+  a.T = 1;
+  a.causal = 0;
+  a.chunk = attn::decode_chunk(B, Hq, Hkv, 1, Lmax);
   a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   const size_t rows = (size_t)B * Hq * a.nsplit;
+  size_t o_bytes = (rows * (size_t)D * sizeof(float) + 255) / 256 * 256;
+  a.part_o = static_cast<float *>(workspace);
+  a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+  return from_cuda(attn::launch_decode(a, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_decode_multi(const void *q, const void *kcache, const void *vcache, const int32_t *seqlens, void *o,
+                              float *lse, int B, int Hq, int Hkv, int T, int Lmax, int D, int causal, float scale,
+                              void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !kcache || !vcache || !seqlens || !o || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || D < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (T < 1 || T > 16) return ATTN_ERR_UNSUPPORTED;
+  if (bad_scale(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_decode_multi_workspace_bytes(B, Hq, Hkv, T, Lmax, D)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hkv > (1LL << 30) || (int64_t)B * Hq * T > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
+  if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
+  CUtensorMap tk, tv;
+  if (!make_tmap(&tk, kcache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Lmax, (uint64_t)B * Hkv, 64, 64) ||
+      !make_tmap(&tv, vcache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Lmax, (uint64_t)B * Hkv, 64, 64))
+    return ATTN_ERR_CUDA;
+  attn::DecodeArgs a{};
+  a.q = q;
+  a.seqlens = seqlens;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.D = D;
+  a.T = T;
+  a.causal = causal ? 1 : 0;
+  a.chunk = attn::decode_chunk(B, Hq, Hkv, T, Lmax);
+  a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
+  a.scale = scale;
+  a.timeout_ns = kDefaultTimeoutNs;
+  a.err = error_word();
+  if (!a.err) return ATTN_ERR_CUDA;
+  const size_t rows = (size_t)B * Hq * T * a.nsplit;
   size_t o_bytes = (rows * (size_t)D * sizeof(float) + 255) / 256 * 256;
   a.part_o = static_cast<float *>(workspace);
   a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);

@@ -59,6 +59,9 @@ struct Params {
   float *part_o;
   float *part_lse;
   int B, Hq, Hkv, Lmax, chunk, nsplit, g, nhc;
+  int T;       // query tokens per sequence (1 = plain decode)
+  int nhpc;    // query heads per CTA: nhpc * T <= 16 MMA rows
+  int causal;  // T > 1: token t sits at position L - T + t and sees keys <= it
   float scale_log2;
   uint64_t timeout_ns;
   unsigned *err;
@@ -96,8 +99,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (s0 >= L) return;  // the whole CTA leaves together, before any barrier
   const int s1 = min(s0 + p.chunk, L);
   const int nst = (s1 - s0 + KS - 1) / KS;
-  const int h0 = kvh * p.g + hc * MROWS;
-  const int nh = min(MROWS, p.g - hc * MROWS);
+  const int T = p.T;
+  const int h0 = kvh * p.g + hc * p.nhpc;
+  const int nh = min(p.nhpc, p.g - hc * p.nhpc);
+  const int nrows = nh * T;  // MMA row r = (query head h0 + r / T, token r % T)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -187,12 +192,16 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int gid = lane >> 2, tq = lane & 3;
   const int mat = lane >> 3, r8 = lane & 7;
 
-  // Q as the A operand: row r = query head h0 + r (rows >= nh are zero).
+  // Q as the A operand: row r = (query head h0 + r / T, token r % T); rows
+  // >= nrows are zero.  q is [B, Hq, T, D].
   uint32_t qa[C::NK][4];
   {
-    const bool ok0 = gid < nh, ok1 = gid + 8 < nh;
-    const uint32_t *q0 = reinterpret_cast<const uint32_t *>(p.q + ((size_t)b * p.Hq + h0 + (ok0 ? gid : 0)) * D);
-    const uint32_t *q1 = reinterpret_cast<const uint32_t *>(p.q + ((size_t)b * p.Hq + h0 + (ok1 ? gid + 8 : 0)) * D);
+    const bool ok0 = gid < nrows, ok1 = gid + 8 < nrows;
+    const int r0 = ok0 ? gid : 0, r1 = ok1 ? gid + 8 : 0;
+    const uint32_t *q0 =
+        reinterpret_cast<const uint32_t *>(p.q + (((size_t)b * p.Hq + h0 + r0 / T) * T + r0 % T) * D);
+    const uint32_t *q1 =
+        reinterpret_cast<const uint32_t *>(p.q + (((size_t)b * p.Hq + h0 + r1 / T) * T + r1 % T) * D);
 #pragma unroll
     for (int ks = 0; ks < C::NK; ++ks) {
       qa[ks][0] = ok0 ? q0[ks * 8 + tq] : 0u;
@@ -205,6 +214,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   float oacc[C::NT][4];
 #pragma unroll
   for (int i = 0; i < C::NT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  // last key each of this lane's two rows may see (bottom-right causal for T > 1)
+  const int lim[2] = {p.causal ? L - T + gid % T : L - 1, p.causal ? L - T + (gid + 8) % T : L - 1};
   float m[2] = {-CUDART_INF_F, -CUDART_INF_F};  // running max (log2 units), rows gid and gid+8
   float l[2] = {0.f, 0.f};                       // running sum, this lane's share
 
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int key = base + kb + nt * 8 + 2 * tq + (i & 1);
-          const float v = key < s1 ? s[nt][i] * p.scale_log2 : -CUDART_INF_F;
+          const float v = (key < s1 && key <= lim[i >> 1]) ? s[nt][i] * p.scale_log2 : -CUDART_INF_F;
           s[nt][i] = v;
           mx[i >> 1] = fmaxf(mx[i >> 1], v);
         }
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   }
   if (!consumers_sync()) return;
-  for (int idx = threadIdx.x; idx < nh * D; idx += NCW * 32) {
+  for (int idx = threadIdx.x; idx < nrows * D; idx += NCW * 32) {
     const int row = idx / D, d = idx % D;
     float M = -CUDART_INF_F;
 #pragma unroll
@@ -348,9 +359,11 @@ __global__ void __launch_bounds__(THREADS, 2)
       tot += f * sl[w * MROWS + row];
       acc += f * so[(w * MROWS + row) * D + d];
     }
-    const size_t ri = ((size_t)b * p.Hq + h0 + row) * p.nsplit + split;
-    p.part_o[ri * D + d] = acc / tot;
-    if (d == 0) p.part_lse[ri] = M + __log2f(tot);
+    // partial rows are (b, head, token), splits innermost
+    const size_t ri = ((((size_t)b * p.Hq + h0 + row / T) * T + row % T) * p.nsplit) + split;
+    const bool empty_row = !(tot > 0.f);  // no key of this split is visible to the row
+    p.part_o[ri * D + d] = empty_row ? 0.f : acc / tot;
+    if (d == 0) p.part_lse[ri] = empty_row ? -CUDART_INF_F : M + __log2f(tot);
   }
 }
 
@@ -360,14 +373,14 @@ struct CombineParams {
   const float *part_lse;
   __nv_bfloat16 *o;
   float *lse;
-  int Hq, Lmax, chunk, nsplit;
+  int Hq, T, Lmax, chunk, nsplit;
 };
 
 // One CTA per (sequence, query head), one thread per output column.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(CombineParams p) {
-  const int bh = blockIdx.x;
-  const int b = bh / p.Hq;
+  const int bh = blockIdx.x;  // (b, head, token) row
+  const int b = bh / (p.Hq * p.T);
   const int d = threadIdx.x;
   griddep_wait();  // launched early (programmatic dependent launch): wait for the splits
   const int L = max(0, min(p.seqlens[b], p.Lmax));
@@ -381,6 +394,11 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(CombineParams p) {
   const float *po = p.part_o + (size_t)bh * p.nsplit * D;
   float M = -CUDART_INF_F;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, pl[s]);
+  if (M == -CUDART_INF_F) {  // the row sees no key (a causal token before the cache start)
+    p.o[(size_t)bh * D + d] = __float2bfloat16(0.f);
+    if (d == 0 && p.lse) p.lse[bh] = -CUDART_INF_F;
+    return;
+  }
   float tot = 0.f, acc = 0.f;
   for (int s = 0; s < ns; ++s) {
     const float w = exp2f(pl[s] - M);
@@ -395,7 +413,8 @@ template <int D, bool PAGED>
 cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv, cudaStream_t st) {
   using C = Cfg<D>;
   const int g = a.Hq / a.Hkv;
-  const int nhc = (g + MROWS - 1) / MROWS;
+  const int nhpc = decode_heads_per_cta(a.Hq, a.Hkv, a.T);
+  const int nhc = (g + nhpc - 1) / nhpc;
   Params p;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.seqlens = a.seqlens;
@@ -413,6 +432,9 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   p.nsplit = a.nsplit;
   p.g = g;
   p.nhc = nhc;
+  p.T = a.T;
+  p.nhpc = nhpc;
+  p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
   p.err = a.err;
@@ -431,11 +453,12 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   c.o = static_cast<__nv_bfloat16 *>(a.o);
   c.lse = a.lse;
   c.Hq = a.Hq;
+  c.T = a.T;
   c.Lmax = a.Lmax;
   c.chunk = a.chunk;
   c.nsplit = a.nsplit;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * a.Hq);
+  cfg.gridDim = dim3(a.B * a.Hq * a.T);
   cfg.blockDim = dim3(D);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
@@ -449,9 +472,10 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
 
 }  // namespace dec
 
-int decode_chunk(int B, int Hq, int Hkv, int Lmax) {
+int decode_chunk(int B, int Hq, int Hkv, int T, int Lmax) {
   const int g = Hq / Hkv;
-  const long units = (long)B * Hkv * ((g + dec::MROWS - 1) / dec::MROWS);
+  const int nhpc = decode_heads_per_cta(Hq, Hkv, T);
+  const long units = (long)B * Hkv * ((g + nhpc - 1) / nhpc);
   long ns = (dec::TARGET_CTAS + units - 1) / units;
   if (ns < 1) ns = 1;
   long chunk = (Lmax + ns - 1) / ns;

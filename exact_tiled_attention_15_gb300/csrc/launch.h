@@ -8,8 +8,14 @@
 
 namespace attn {
 
-// Keys per split of the decode kernel for these sizes (a multiple of 64).
-int decode_chunk(int B, int Hq, int Hkv, int Lmax);
+// Query heads one decode CTA covers: nhpc * T query rows fit the 16 MMA rows.
+inline int decode_heads_per_cta(int Hq, int Hkv, int T) {
+  const int g = Hq / Hkv, n = 16 / T;
+  return n < g ? n : g;
+}
+// Keys per split of the decode kernel for these sizes (a multiple of 64);
+// T = query tokens per sequence.
+int decode_chunk(int B, int Hq, int Hkv, int T, int Lmax);
 // Number of key splits for a cache of Lmax rows.
 inline int decode_nsplit(int Lmax, int chunk) { return (Lmax + chunk - 1) / chunk; }
 
@@ -23,6 +29,7 @@ struct DecodeArgs {
   float *part_o;    // [B, Hq, nsplit, D]
   float *part_lse;  // [B, Hq, nsplit], log2 domain
   int B, Hq, Hkv, Lmax, D, chunk, nsplit;
+  int T, causal;  // query tokens per sequence; bottom-right causal mask among them
   float scale;
   uint64_t timeout_ns;
   unsigned *err;

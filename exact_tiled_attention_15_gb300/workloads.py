@@ -64,7 +64,7 @@ def make_prefill(B, Hq, Hkv, Sq, Sk, D, seed=0, k_outlier_frac=0.0, k_outlier_mu
     return dict(q=to_bf16(q), k=to_bf16(k), v=to_bf16(v))
 
 
-def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True, seqlens=None):
+def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True, seqlens=None, T=None):
     """One query token per sequence against a contiguous per-sequence KV cache.
 
     Returns q [B,Hq,D] bf16, kcache/vcache [B,Hkv,Lmax,D] bf16 and seqlens [B]
@@ -73,12 +73,13 @@ def make_decode(B, Hq, Hkv, D, Lmin, Lmax, seed=0, poison_tail=True, seqlens=Non
     Only the live cache rows (position < seqlens[b]) are drawn: first all of
     K's, in (b, head, position, d) order, then all of V's.  Rows at or beyond a
     sequence's length are NaN when ``poison_tail`` (so any read of them shows
-    up in the output), else 0.
+    up in the output), else 0.  With T, q holds T query tokens per sequence:
+    [B, Hq, T, D].
     """
     rng = np.random.default_rng(seed)
     drawn = rng.integers(Lmin, Lmax + 1, size=B).astype(np.int32)
     seqlens = drawn if seqlens is None else np.asarray(seqlens, dtype=np.int32)
-    q = rng.standard_normal((B, Hq, D), dtype=np.float32)
+    q = rng.standard_normal((B, Hq, D) if T is None else (B, Hq, T, D), dtype=np.float32)
     fill = np.nan if poison_tail else 0.0
     caches = []
     for _ in range(2):  # K, then V

@@ -99,6 +99,33 @@ attn_status attn_decode(const void *q, const void *kcache, const void *vcache,
                         void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_multi_workspace_bytes -- scratch for attn_decode_multi (0 on
+ * invalid sizes).
+ */
+size_t attn_decode_multi_workspace_bytes(int B, int Hq, int Hkv, int T, int Lmax, int D);
+
+/*
+ * attn_decode_multi -- T query tokens per sequence against its KV cache: the
+ * verification step of speculative decoding, or a short chunk of prefill
+ * ("Week 13. GPUs and FlashAttention", step 1: draft verification scores
+ * gamma + 1 tokens per sequence in one pass).  The cache already holds the T
+ * new tokens' K and V (seqlens[b] counts them).
+ *   q [B, Hq, T, D] bf16, o [B, Hq, T, D] bf16, lse [B, Hq, T] fp32 (may be NULL)
+ *   kcache, vcache [B, Hkv, Lmax, D] bf16, seqlens [B] int32 as for attn_decode.
+ *   1 <= T <= 16 (else ATTN_ERR_UNSUPPORTED).
+ *   causal != 0: token t sits at position seqlens[b] - T + t and sees keys at
+ *           positions <= its own (bottom-right alignment); a token whose
+ *           position is negative sees nothing (O = 0, LSE = -inf).
+ *           causal == 0: every token sees all seqlens[b] keys.
+ *   workspace: at least attn_decode_multi_workspace_bytes(B, Hq, Hkv, T, Lmax, D)
+ *           bytes, 256-byte aligned.
+ * With T = 1 this is attn_decode.
+ */
+attn_status attn_decode_multi(const void *q, const void *kcache, const void *vcache, const int32_t *seqlens,
+                              void *o, float *lse, int B, int Hq, int Hkv, int T, int Lmax, int D, int causal,
+                              float scale, void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_decode_paged -- attn_decode against a paged KV cache ("Fast Inference
  * and Training at Scale" §6.3, PagedAttention: the cache lives in fixed-size
  * blocks reached through a per-sequence block table).

@@ -22,6 +22,6 @@ Every function states the passage it follows.  Pins (tests/test_oracle.py)
 check each against invariants, closed forms, brute force and library
 routines.
 """
-from .attention import attention, attention_rows, decode, decode_paged, merge_partials  # noqa: F401
+from .attention import attention, attention_rows, decode, decode_multi, decode_paged, merge_partials  # noqa: F401
 from .codecs import bf16_decode, e4m3_decode, dequantize_tiles  # noqa: F401
 from .online import attention_online  # noqa: F401

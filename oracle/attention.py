@@ -162,3 +162,26 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, page_size: int, scal
             kc[b, :, t] = np.asarray(k_pages[page, :, t % page_size], dtype=np.float64)
             vc[b, :, t] = np.asarray(v_pages[page, :, t % page_size], dtype=np.float64)
     return decode(q, kc, vc, seqlens, scale)
+
+
+def decode_multi(q, kcache, vcache, seqlens, causal: bool = True, scale: float | None = None):
+    """T query tokens per sequence against its cache: q [B,Hq,T,D],
+    cache [B,Hkv,Lmax,D].  The tokens are the last T positions of the
+    sequence (its cache already holds their K and V), so with the causal mask
+    token t (position seqlens[b] - T + t) sees keys up to its own position --
+    the bottom-right alignment of `attention` with Sq = T, Sk = seqlens[b].
+    This is the verification pass of speculative decoding ("Week 13. GPUs and
+    FlashAttention", step 1: gamma + 1 tokens per sequence in one pass).
+    Returns O [B,Hq,T,D], LSE [B,Hq,T].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, T, D = q.shape
+    O = np.zeros((B, Hq, T, D))
+    L = np.full((B, Hq, T), -np.inf)
+    for b in range(B):
+        n = int(seqlens[b])
+        if n <= 0:
+            continue
+        O[b:b + 1], L[b:b + 1] = attention(q[b:b + 1], np.asarray(kcache[b:b + 1, :, :n], dtype=np.float64),
+                                           np.asarray(vcache[b:b + 1, :, :n], dtype=np.float64), causal, scale)
+    return O, L

@@ -251,6 +251,34 @@ def test_paged_decode_gathers_pages_in_position_order():
         assert not np.array_equal(np.sort(w["block_table"].numpy().ravel()), w["block_table"].numpy().ravel())
 
 
+def test_multi_token_decode():
+    """T = 1 is decode; with the causal mask the last token sees the whole
+    cache and token t sees exactly the first L - T + t + 1 keys (brute force);
+    a token before the cache start sees nothing."""
+    w1 = workloads.make_decode(B=3, Hq=8, Hkv=2, D=16, Lmin=5, Lmax=60, seed=41, T=1)
+    q1 = w1["q"].double().numpy()
+    kc, vc, sl = w1["kcache"].double().numpy(), w1["vcache"].double().numpy(), w1["seqlens"].numpy()
+    O1, L1 = oracle.decode_multi(q1, kc, vc, sl)
+    Od, Ld = oracle.decode(q1[:, :, 0], kc, vc, sl)
+    np.testing.assert_allclose(O1[:, :, 0], Od, atol=TOL)
+    np.testing.assert_allclose(L1[:, :, 0], Ld, atol=TOL)
+    w = workloads.make_decode(B=3, Hq=8, Hkv=2, D=16, Lmin=2, Lmax=60, seed=42, T=5, seqlens=[2, 17, 60])
+    q = w["q"].double().numpy()
+    kc, vc, sl = w["kcache"].double().numpy(), w["vcache"].double().numpy(), w["seqlens"].numpy()
+    O, L = oracle.decode_multi(q, kc, vc, sl, causal=True)
+    On, Ln = oracle.decode_multi(q, kc, vc, sl, causal=False)
+    np.testing.assert_allclose(O[:, :, -1], On[:, :, -1], atol=TOL)
+    for b in range(3):
+        for t in range(5):
+            n = int(sl[b]) - 5 + t + 1
+            if n <= 0:
+                assert (O[b, :, t] == 0).all() and np.isneginf(L[b, :, t]).all()
+                continue
+            Ob, Lb = oracle.decode(q[b:b + 1, :, t], kc[b:b + 1, :, :n], vc[b:b + 1, :, :n], np.array([n]))
+            np.testing.assert_allclose(O[b, :, t], Ob[0], atol=TOL)
+            np.testing.assert_allclose(L[b, :, t], Lb[0], atol=TOL)
+
+
 # ---------------------------------------------------------------- codecs
 def test_bf16_decoder_matches_library_cast():
     codes = np.arange(1 << 16, dtype=np.uint16)
