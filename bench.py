@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--only", choices=["train_prefill_mha", "long_gqa_prefill", "gqa_decode", "gqa_decode_paged",
-                                       "gqa_decode_T4", "fp8_prefill"],
+                                       "gqa_decode_T4", "fp8_rotate_quantize", "fp8_prefill"],
                     help="run one workload leg alone and print its figures (for profiling)")
     return ap.parse_args()
 
@@ -356,6 +356,42 @@ def run_decode_multi(steps, warmup, flush, peaks, T=4):
     }
 
 
+def run_quant(steps, warmup, flush, peaks):
+    """Rotate + quantise Q, K (with signs) and V (without) of the FP8 workload."""
+    import numpy as np
+    import torch
+    import exact_tiled_attention_15_gb300 as eta
+    from exact_tiled_attention_15_gb300 import workloads
+    cfg = workloads.WORKLOADS["fp8_prefill"]
+    B, H, S, D = cfg["B"], cfg["Hq"], cfg["S"], cfg["D"]
+    w = workloads.make_prefill(B, H, H, S, S, D, seed=0)
+    dev = torch.device("cuda")
+    xs = [w[n].to(dev) for n in ("q", "k", "v")]
+    signs = torch.from_numpy(np.random.default_rng(0).integers(0, 2, D).astype(np.float32) * 2 - 1).to(dev)
+    outs = [(torch.empty(B, H, S, D, dtype=torch.uint8, device=dev),
+             torch.empty(B, H, -(-S // 128), 1, dtype=torch.float32, device=dev)) for _ in range(3)]
+
+    def fn():
+        for x, sg, (c, sc) in zip(xs, (signs, signs, None), outs):
+            eta.rotate_quantize_fp8(x, sg, codes=c, scales=sc)
+
+    ts = time_steps(fn, steps, warmup, flush)
+    if eta.get_error() != 0:
+        raise RuntimeError("rotate+quantise: device-side error")
+    nbytes = 3 * (B * H * S * D * 3 + B * H * (-(-S // 128)) * 4)  # bf16 read + code write + scales
+    ms = statistics.mean(ts)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": "GB/s (Hadamard rotate + per-tile e4m3 quantise of Q, K, V)", "unit": "GB/s", "value": gbs,
+        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "config": {"workload": "fp8_prefill inputs", "B": B, "H": H, "S": S, "D": D, "tensors": 3},
+        "roofline": {"bound": "hbm", "kernel": "rotate_quantize_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " HBM copy",
+                     "traffic": None, "algorithmic_bytes": nbytes},
+        "gpu_launches": 3 * len(ts),
+    }
+
+
 def run_fp8(steps, warmup, flush, peaks):
     import torch
     import exact_tiled_attention_15_gb300 as eta
@@ -468,6 +504,8 @@ def main():
             res = run_decode(args.steps, args.warmup, flush, peaks)
         elif args.only == "gqa_decode_paged":
             res = run_decode_paged(args.steps, args.warmup, flush, peaks)
+        elif args.only == "fp8_rotate_quantize":
+            res = run_quant(args.steps, args.warmup, flush, peaks)
         elif args.only == "gqa_decode_T4":
             res = run_decode_multi(args.steps, args.warmup, flush, peaks, T=4)
         elif args.only == "fp8_prefill":
@@ -494,6 +532,7 @@ def main():
         extras["gqa_decode"] = run_decode(args.steps, args.warmup, flush, peaks)
         extras["gqa_decode_paged"] = run_decode_paged(args.steps, args.warmup, flush, peaks)
         extras["gqa_decode_T4"] = run_decode_multi(args.steps, args.warmup, flush, peaks, T=4)
+        extras["fp8_rotate_quantize"] = run_quant(args.steps, args.warmup, flush, peaks)
         try:
             extras["fp8_prefill"] = run_fp8(args.steps, args.warmup, flush, peaks)
         except Exception as e:  # reported, not hidden

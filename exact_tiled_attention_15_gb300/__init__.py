@@ -7,8 +7,9 @@
 ``decode_paged``  the same against a paged KV cache (block table) -> (O, LSE)
 ``decode_multi``  T <= 16 query tokens per sequence (speculative verification) -> (O, LSE)
 ``fwd_fp8``  FP8 e4m3 prefill with one scale per 128x128 tile -> (O, LSE)
+``rotate_quantize_fp8``  Hadamard rotation + per-tile e4m3 quantisation of its inputs
 
 All three call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import AttnError, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, version  # noqa: F401
+from ._lib import AttnError, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, rotate_quantize_fp8, version  # noqa: F401

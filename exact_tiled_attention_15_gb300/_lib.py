@@ -31,6 +31,7 @@ SIGNATURES = {
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_rotate_quantize_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_get_error": (_I, [_P]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
     "attn_version": (ctypes.c_char_p, []),
@@ -245,6 +246,24 @@ def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, ret
                             _stream(q8.device))
     _check(st, "attn_fwd_fp8")
     return o, lse
+
+
+def rotate_quantize_fp8(x, signs=None, codes=None, scales=None):
+    """bf16 x [B,H,S,128] -> (e4m3 codes uint8 [B,H,S,128], scales fp32 [B,H,ceil(S/128),1]).
+    With signs ([128] float32 of +-1) the rows are first multiplied by H_128 diag(signs) / sqrt(128)."""
+    _need(x, "x", torch.bfloat16, 4)
+    B, H, S, D = x.shape
+    if signs is not None:
+        _need(signs, "signs", torch.float32, 1)
+        if signs.shape[0] != D:
+            raise ValueError("signs must have D entries")
+    codes = codes if codes is not None else torch.empty(B, H, S, D, device=x.device, dtype=torch.uint8)
+    scales = scales if scales is not None else torch.empty(B, H, -(-S // 128), 1, device=x.device,
+                                                           dtype=torch.float32)
+    st = lib().attn_rotate_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), _ptr(signs), B, H, S, D,
+                                        _stream(x.device))
+    _check(st, "attn_rotate_quantize_fp8")
+    return codes, scales
 
 
 def get_error(device=None) -> int:

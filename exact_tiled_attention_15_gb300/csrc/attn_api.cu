@@ -340,6 +340,20 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
   return from_cuda(attn::launch_fwd_fp8(a, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
+                                     int S, int D, attn_stream_t stream) {
+  if (!x || !codes || !scales) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
+      (signs && (reinterpret_cast<uintptr_t>(signs) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
+  return from_cuda(attn::launch_rotate_quantize(x, codes, scales, signs, B, H, S,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 attn_status attn_get_error(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
   unsigned *p = error_word();

@@ -60,4 +60,9 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tmap_q, const C
 cudaError_t launch_fwd_fp8(const FwdArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
                            const CUtensorMap &tmap_v, cudaStream_t stream);
 
+// Hadamard rotation (signs != nullptr) + per-128x128-tile e4m3 quantisation of a
+// bf16 [B, H, S, 128] tensor.
+cudaError_t launch_rotate_quantize(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
+                                   int S, cudaStream_t stream);
+
 }  // namespace attn

@@ -196,6 +196,23 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
                          int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_rotate_quantize_fp8 -- prepares attn_fwd_fp8's inputs: optional Hadamard
+ * rotation, then block quantisation to e4m3 with one fp32 scale per 128 x 128
+ * tile ("FlashAttention scaling, multi-GPU training and weight quantization"
+ * §1, FlashAttention-3: incoherent processing and block quantisation).
+ *   x      [B, H, S, D] bf16 (D == 128 only)
+ *   signs  [D] fp32 of +-1, or NULL for no rotation (use NULL for V and the
+ *          same signs for Q and K, which leaves Q K^T unchanged)
+ *   codes  [B, H, S, D] e4m3 bytes (written)
+ *   scales [B, H, ceil(S/128), 1] fp32 (written)
+ * With signs, y = x R, R = H_D diag(signs) / sqrt(D) (Sylvester Hadamard);
+ * else y = x.  Per tile: scale = max |y| / 448 (1 if the tile is all zero),
+ * code = e4m3(y / scale), nearest even, saturating at +-448.
+ */
+attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
+                                     int S, int D, attn_stream_t stream);
+
+/*
  * attn_get_error -- synchronises `stream`, then returns and clears the device
  * error word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a bounded
  * pipeline wait ran out since the last call (its kernel then returned early

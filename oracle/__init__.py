@@ -17,6 +17,8 @@ Contents
                 attention.py.
   codecs.py     bf16 and FP8 e4m3 decoders written from the formats' bit
                 layouts, and the per-tile dequantisation of FP8 inputs.
+  quant.py      the e4m3 encoder and the Hadamard-rotate + per-tile e4m3
+                quantisation step of FlashAttention-3's FP8 path.
 
 Every function states the passage it follows.  Pins (tests/test_oracle.py)
 check each against invariants, closed forms, brute force and library
@@ -25,3 +27,4 @@ routines.
 from .attention import attention, attention_rows, decode, decode_multi, decode_paged, merge_partials  # noqa: F401
 from .codecs import bf16_decode, e4m3_decode, dequantize_tiles  # noqa: F401
 from .online import attention_online  # noqa: F401
+from .quant import e4m3_encode, rotate_quantize  # noqa: F401

@@ -316,6 +316,41 @@ def test_dequantize_tiles_matches_library_and_scale_layout():
         assert blk.max() == 448.0
 
 
+def test_e4m3_encoder_matches_library_cast_including_ties():
+    decoded = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))       # +0 .. 448
+    mids = (decoded[:-1] + decoded[1:]) / 2                              # exact ties
+    rng = np.random.default_rng(43)
+    vals = np.concatenate([decoded, mids, -mids, rng.uniform(-448, 448, 20000), rng.normal(0, 1e-2, 5000),
+                           [448.0, -448.0, 0.0]])
+    ours = oracle.e4m3_encode(vals)
+    lib = torch.from_numpy(vals.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # torch rounds from float32; every value above is exact in float32
+    np.testing.assert_array_equal(ours, lib)
+    np.testing.assert_array_equal(oracle.e4m3_decode(oracle.e4m3_encode(decoded)), decoded)
+    assert oracle.e4m3_encode([1e6])[0] == 0x7E and oracle.e4m3_encode([-1e6])[0] == 0xFE   # saturate
+
+
+def test_rotate_quantize_round_trip_and_tile_scales():
+    rng = np.random.default_rng(44)
+    x = rng.standard_normal((1, 2, 300, 128))
+    x[0, 0, 5, 7] = 40.0                                                  # an outlier
+    signs = rng.integers(0, 2, 128) * 2.0 - 1.0
+    codes, scales, y = oracle.rotate_quantize(x, signs)
+    assert scales.shape == (1, 2, 3, 1)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)  # orthogonal
+    deq = oracle.dequantize_tiles(codes, scales)
+    R = oracle.quant.hadamard(128) * signs[None, :] / np.sqrt(128)
+    back = deq @ R.T
+    assert np.linalg.norm(back - x) / np.linalg.norm(x) < 0.04          # e4m3 keeps ~3 significant bits
+    for t in range(3):                                                    # each tile's largest |y| -> 448
+        assert np.abs(oracle.e4m3_decode(codes[0, 0, t * 128:(t + 1) * 128])).max() == 448.0
+    # the rotation spreads the outlier over the row: the tile's largest magnitude drops
+    c0, s0, _ = oracle.rotate_quantize(x, None)
+    assert np.abs(y[0, 0, :128]).max() < 0.5 * np.abs(x[0, 0, :128]).max()
+    assert scales[0, 0, 0, 0] < 0.5 * s0[0, 0, 0, 0]
+    np.testing.assert_array_equal(c0, oracle.e4m3_encode(x / np.repeat(s0, 128, 2)[:, :, :300]))
+
+
 # ---------------------------------------------------------------- input generator pins
 def test_rotation_is_orthogonal_and_preserves_scores():
     """Incoherent processing (FlashAttention-3): rotating Q and K by the same
