@@ -17,6 +17,8 @@ Contents
                 attention.py.
   codecs.py     bf16 and FP8 e4m3 decoders written from the formats' bit
                 layouts, and the per-tile dequantisation of FP8 inputs.
+  backward.py   the gradients dQ, dK, dV by their definition (recomputing P
+                from the log-sum-exp).
   quant.py      the e4m3 encoder and the Hadamard-rotate + per-tile e4m3
                 quantisation step of FlashAttention-3's FP8 path.
 
@@ -28,3 +30,4 @@ from .attention import attention, attention_rows, decode, decode_multi, decode_p
 from .codecs import bf16_decode, e4m3_decode, dequantize_tiles  # noqa: F401
 from .online import attention_online  # noqa: F401
 from .quant import e4m3_encode, rotate_quantize  # noqa: F401
+from .backward import attention_backward  # noqa: F401

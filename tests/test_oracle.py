@@ -279,6 +279,56 @@ def test_multi_token_decode():
             np.testing.assert_allclose(L[b, :, t], Lb[0], atol=TOL)
 
 
+def _loss(q, k, v, do, causal, scale):
+    O, _ = oracle.attention(q, k, v, causal=causal, scale=scale)
+    return float((O * do).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    """Central differences of sum(dO o O) in float64 pin every gradient entry
+    of a tiny GQA case (2 query heads on 1 KV head, Sq != Sk)."""
+    q, k, v = rand(1, 2, 4, 3, seed=50), rand(1, 1, 6, 3, seed=51), rand(1, 1, 6, 3, seed=52)
+    do = rand(1, 2, 4, 3, seed=53)
+    dq, dk, dv, _, _ = oracle.attention_backward(q, k, v, do, causal=causal, scale=0.7)
+    h = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [xp if y is x else y for y in (q, k, v)]
+            args_m = [xm if y is x else y for y in (q, k, v)]
+            num[idx] = (_loss(*args_p, do, causal, 0.7) - _loss(*args_m, do, causal, 0.7)) / (2 * h)
+        np.testing.assert_allclose(g, num, atol=1e-7, rtol=1e-6)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_library_autograd(causal):
+    """PyTorch's CPU fp64 autograd through scaled_dot_product_attention (test
+    only), with grouped-query heads."""
+    q, k, v = rand(2, 4, 33, 16, seed=54), rand(2, 2, 33, 16, seed=55), rand(2, 2, 33, 16, seed=56)
+    do = rand(2, 4, 33, 16, seed=57)
+    dq, dk, dv, _, _ = oracle.attention_backward(q, k, v, do, causal=causal)
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_() for x in (q, k, v))
+    F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, enable_gqa=True).backward(torch.from_numpy(do))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-10)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-10)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-10)
+
+
+def test_backward_gqa_is_group_sum_of_mha():
+    q = rand(1, 4, 20, 8, seed=58)
+    k, v = rand(1, 2, 20, 8, seed=59), rand(1, 2, 20, 8, seed=60)
+    do = rand(1, 4, 20, 8, seed=61)
+    dq, dk, dv, _, _ = oracle.attention_backward(q, k, v, do, causal=True)
+    dq2, dk2, dv2, _, _ = oracle.attention_backward(q, np.repeat(k, 2, 1), np.repeat(v, 2, 1), do, causal=True)
+    np.testing.assert_allclose(dq, dq2, atol=TOL)
+    np.testing.assert_allclose(dk, dk2.reshape(1, 2, 2, 20, 8).sum(2), atol=TOL)
+    np.testing.assert_allclose(dv, dv2.reshape(1, 2, 2, 20, 8).sum(2), atol=TOL)
+
+
 # ---------------------------------------------------------------- codecs
 def test_bf16_decoder_matches_library_cast():
     codes = np.arange(1 << 16, dtype=np.uint16)
