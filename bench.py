@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--only", choices=["train_prefill_mha", "long_gqa_prefill", "gqa_decode", "gqa_decode_paged",
+    ap.add_argument("--only", choices=["train_prefill_mha", "train_prefill_mha_backward", "long_gqa_prefill",
+                                       "gqa_decode", "gqa_decode_paged",
                                        "gqa_decode_T4", "fp8_rotate_quantize", "fp8_prefill"],
                     help="run one workload leg alone and print its figures (for profiling)")
     return ap.parse_args()
@@ -247,6 +248,42 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
                       "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4, "steps": len(te)}
     del q, k, v, o, lse
     return res
+
+
+def run_backward(steps, warmup, flush, peaks):
+    """Gradients of the headline causal prefill (dQ, dK, dV from Q, K, V, O,
+    LSE and a random dO)."""
+    import numpy as np
+    import torch
+    import exact_tiled_attention_15_gb300 as eta
+    from exact_tiled_attention_15_gb300 import accounting as acc, workloads
+    name = HEADLINE
+    cfg = workloads.WORKLOADS[name]
+    B, Hq, Hkv, S, D, causal = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["D"], cfg["causal"]
+    w = workloads.make_workload(name, seed=0)
+    dev = torch.device("cuda")
+    q, k, v = (w[n].to(dev) for n in ("q", "k", "v"))
+    do = workloads.to_bf16(np.random.default_rng(7).standard_normal((B, Hq, S, D)).astype(np.float32)).to(dev)
+    o, lse = eta.fwd(q, k, v, causal=causal)
+    ws = torch.empty(int(eta.lib().attn_bwd_workspace_bytes(B, Hq, S, D)), dtype=torch.uint8, device=dev)
+    fn = lambda: eta.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws)  # noqa: E731
+    ts = time_steps(fn, steps, warmup, flush)
+    if eta.get_error() != 0:
+        raise RuntimeError("backward: device-side error")
+    flops = acc.backward_flops(B, Hq, S, S, D, causal)
+    ms = statistics.mean(ts)
+    ach = flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": "attention backward TFLOP/s (bf16, recomputation)", "unit": "TFLOP/s", "value": ach,
+        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "config": {"workload": name + "_backward", "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Sk": S, "D": D,
+                   "causal": causal},
+        "roofline": {"bound": "tensor", "kernel": "bwd_pre + bwd_kernel<128> + bwd_post", "achieved": ach,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                     "peak_source": peaks["source"] + " bf16 burst", "traffic": None,
+                     "algorithmic_flops": flops},
+        "gpu_launches": 3 * len(ts),
+    }
 
 
 def run_decode(steps, warmup, flush, peaks):
@@ -502,6 +539,8 @@ def main():
     if args.only:
         if args.only == "gqa_decode":
             res = run_decode(args.steps, args.warmup, flush, peaks)
+        elif args.only == "train_prefill_mha_backward":
+            res = run_backward(args.steps, args.warmup, flush, peaks)
         elif args.only == "gqa_decode_paged":
             res = run_decode_paged(args.steps, args.warmup, flush, peaks)
         elif args.only == "fp8_rotate_quantize":
@@ -529,6 +568,7 @@ def main():
     extras = {}
     if not args.no_extras:
         extras["long_gqa_prefill"] = run_prefill("long_gqa_prefill", max(5, args.steps // 4), args.warmup, flush, peaks)
+        extras["train_prefill_mha_backward"] = run_backward(max(5, args.steps // 4), args.warmup, flush, peaks)
         extras["gqa_decode"] = run_decode(args.steps, args.warmup, flush, peaks)
         extras["gqa_decode_paged"] = run_decode_paged(args.steps, args.warmup, flush, peaks)
         extras["gqa_decode_T4"] = run_decode_multi(args.steps, args.warmup, flush, peaks, T=4)

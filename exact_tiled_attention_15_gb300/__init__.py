@@ -3,6 +3,7 @@
     from exact_tiled_attention_15_gb300 import fwd, decode, fwd_fp8
 
 ``fwd``      bf16 prefill (causal or not, MHA/GQA/MQA) -> (O, LSE)
+``bwd``      its gradients (dQ, dK, dV), recomputing P from LSE
 ``decode``   one query token per sequence against a KV cache -> (O, LSE)
 ``decode_paged``  the same against a paged KV cache (block table) -> (O, LSE)
 ``decode_multi``  T <= 16 query tokens per sequence (speculative verification) -> (O, LSE)
@@ -12,4 +13,4 @@
 All three call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import AttnError, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, rotate_quantize_fp8, version  # noqa: F401
+from ._lib import AttnError, bwd, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, rotate_quantize_fp8, version  # noqa: F401

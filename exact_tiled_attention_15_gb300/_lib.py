@@ -25,6 +25,8 @@ _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode_multi_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_decode_multi": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
@@ -110,6 +112,25 @@ def fwd(q, k, v, causal=False, scale=None, return_lse=True, out=None, lse_out=No
                         1 if causal else 0, scale, _stream(q.device))
     _check(st, "attn_fwd")
     return o, lse
+
+
+def bwd(q, k, v, o, lse, dout, causal=False, scale=None, workspace=None):
+    """Gradients of fwd: (dq, dk, dv) for the given dout, from q, k, v, o and the forward's lse."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, name, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    nbytes = int(lib().attn_bwd_workspace_bytes(B, Hq, Sq, D))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, Hq, Hkv, Sq, Sk, D, 1 if causal else 0, scale, _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(q.device))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def decode_workspace_bytes(B, Hq, Hkv, Lmax, D) -> int:

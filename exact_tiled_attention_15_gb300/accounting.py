@@ -17,6 +17,12 @@ def prefill_flops(B, Hq, Sq, Sk, D, causal) -> float:
     return f / 2 if causal else f
 
 
+def backward_flops(B, Hq, Sq, Sk, D, causal) -> float:
+    """Five products per score (S and dP recomputed, dV, dK, dQ), 2*D FLOPs
+    each: 2.5 x the forward's count."""
+    return 2.5 * prefill_flops(B, Hq, Sq, Sk, D, causal)
+
+
 def prefill_bytes(B, Hq, Hkv, Sq, Sk, D, elem_bytes=2, out_bytes=2, lse=True) -> float:
     qkv = (B * Hq * Sq * D + 2 * B * Hkv * Sk * D) * elem_bytes
     out = B * Hq * Sq * D * out_bytes + (B * Hq * Sq * 4 if lse else 0)

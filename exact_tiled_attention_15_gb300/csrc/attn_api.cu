@@ -340,6 +340,54 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
   return from_cuda(attn::launch_fwd_fp8(a, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
+  if (B < 1 || Hq < 1 || Sq < 1 || D < 1) return 0;
+  const size_t rows = (size_t)B * Hq * Sq;
+  return (rows * D * sizeof(float) + 255) / 256 * 256 + rows * sizeof(float);
+}
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+                     void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                     float scale, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  attn_status st = check_prefill(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale);
+  if (st != ATTN_OK) return st;
+  if (!lse || !dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Sq, D)) return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sq, (uint64_t)B * Hq, 64, 128) ||
+      !make_tmap(&tdo, dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sq, (uint64_t)B * Hq, 64, 128) ||
+      !make_tmap(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sk, (uint64_t)B * Hkv, 64, 128) ||
+      !make_tmap(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sk, (uint64_t)B * Hkv, 64, 128))
+    return ATTN_ERR_CUDA;
+  attn::BwdArgs a{};
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  const size_t rows = (size_t)B * Hq * Sq;
+  a.dq_acc = static_cast<float *>(workspace);
+  a.dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) + (rows * D * sizeof(float) + 255) / 256 * 256);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.D = D;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.timeout_ns = kDefaultTimeoutNs;
+  a.err = error_word();
+  if (!a.err) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_bwd(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
                                      int S, int D, attn_stream_t stream) {
   if (!x || !codes || !scales) return ATTN_ERR_INVALID_ARG;

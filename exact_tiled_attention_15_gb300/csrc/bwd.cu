@@ -1,0 +1,432 @@
+// bwd.cu -- attention backward with recomputation on the sm_103a tensor cores.
+//
+// "Fast Inference and Training at Scale" §6.21 (Idea 2) and "Week 13. GPUs and
+// FlashAttention" step 2: the forward keeps only O and the per-row
+// log-sum-exp; the backward recomputes the scores tile by tile and never
+// stores an S x S matrix.  With S = scale Q K^T, P = exp(S - LSE):
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - rowsum(dO o O)),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Kernel 1 (bwd_pre_kernel): Dvec = rowsum(dO o O) in fp32, and zeroes the fp32
+// dQ accumulator.
+// Kernel 2 (bwd_kernel): one CTA per (128-key tile, KV head, batch) walks
+// every visible 128-row query tile of the KV head's query-head group:
+//   warp 8      TMA: K_j, V_j once; Q_i and dO_i into a 2-stage ring;
+//   warp 9      one thread issues tcgen05.mma:
+//                 S^T = K_j Q_i^T and dP^T = V_j dO_i^T (shared-memory operands,
+//                 fp32 results in TMEM, one lane per key);
+//                 dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T read from TMEM,
+//                 accumulators stay in TMEM for the whole CTA);
+//                 dQ_i = dS K_j (dS staged in shared memory, MN-major);
+//   warps 0-3   one thread per key: P^T = exp2(S^T scale log2e - LSE log2e),
+//               dS^T = P^T o (dP^T - Dvec), written back to TMEM (bf16) and
+//               dS^T to shared memory;
+//   warps 4-7   one thread per query row: read dQ_i from TMEM and add
+//               scale * dQ_i into the fp32 accumulator (vector atomics);
+// then dK (times scale) and dV are written once as bf16.
+// Kernel 3 (bwd_post_kernel): dQ = bf16(accumulator).
+// TMEM columns: S^T [0,128) (then P^T bf16 in [0,64), then dQ_i [0,128)),
+// dP^T [128,256) (then dS^T bf16 in [128,192)), dV [256,384), dK [384,512).
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace bwd {
+
+constexpr int BM = 128;          // query rows per Q tile
+constexpr int BN = 128;          // keys per CTA
+constexpr int NS = 2;            // Q / dO ring depth
+constexpr int HALF = 128 * 128;  // 128 rows x 128 bytes
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int THREADS = 10 * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 384;
+
+template <int D>
+struct Cfg {
+  static constexpr int NH = D / 64;
+  static constexpr int TILE = NH * HALF;  // 128 x D bf16
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;        // NS stages of Q
+  static constexpr int OFF_DO = OFF_Q + NS * TILE;  // NS stages of dO
+  static constexpr int OFF_DS = OFF_DO + NS * TILE; // dS^T staging: 128 keys x 128 queries bf16
+  static constexpr int OFF_BAR = OFF_DS + 2 * HALF;
+  static constexpr int NBAR = 1 + 2 * NS + 5;
+  static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
+  // M = 128; K-major A and B (S^T, dP^T)
+  static constexpr uint32_t IDESC_SS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BM >> 3) << 17) |
+                                       ((uint32_t)(128 >> 4) << 24);
+  // A from TMEM (K-major), B MN-major, N = D (dV, dK)
+  static constexpr uint32_t IDESC_TS = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                       ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  // A and B MN-major, N = D (dQ = dS K)
+  static constexpr uint32_t IDESC_DQ = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
+                                       ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+struct Params {
+  const float *lse;   // [B, Hq, Sq] natural log (forward output)
+  const float *dvec;  // [B, Hq, Sq] rowsum(dO o O)
+  float *dq_acc;      // [B, Hq, Sq, D] fp32
+  __nv_bfloat16 *dk, *dv;
+  int B, Hq, Hkv, Sq, Sk, causal, g, nqt;
+  float scale, scale_log2;
+  uint64_t timeout_ns;
+  unsigned *err;
+};
+
+// Byte offset of the 16-byte chunk c (queries 8c .. 8c+7) of key row k in the
+// dS^T staging buffer (two 64-query slabs, 128-byte rows, 128-byte swizzle).
+__device__ __forceinline__ uint32_t ds_off(int k, int c) {
+  return (c >> 3) * HALF + k * 128 + (((c & 7) ^ (k & 7)) << 4);
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *kv_full = bars;
+  uint64_t *q_full = bars + 1, *q_empty = q_full + NS;
+  uint64_t *st_full = q_empty + NS, *p_ready = st_full + 1, *dq_full = p_ready + 1, *dq_free = dq_full + 1;
+  uint64_t *done_bar = dq_free + 1;
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
+
+  const int j = blockIdx.x;  // key tile
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.Hkv, kvh = bkv % p.Hkv;
+  const int kj0 = j * BN;
+  const int off = p.Sk - p.Sq;  // causal: key k visible to query q iff k <= q + off
+  // query tiles that see at least one key of this tile (a suffix of 0..nqt-1)
+  int qt0 = 0;
+  if (p.causal) {
+    qt0 = max(0, (kj0 - off) / BM - 1);
+    while (qt0 < p.nqt && min(qt0 * BM + BM - 1, p.Sq - 1) + off < kj0) ++qt0;
+  }
+  const int nvis = p.nqt - qt0;
+  const int nitems = nvis * p.g;  // item it: query head kvh*g + it / nvis, query tile qt0 + it % nvis
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (nitems == 0) {  // no query sees these keys: zero gradients
+    for (int idx = threadIdx.x; idx < BN * D / 8; idx += THREADS) {
+      const int k = idx / (D / 8), c = idx % (D / 8);
+      if (kj0 + k < p.Sk) {
+        const size_t o = ((size_t)bkv * p.Sk + kj0 + k) * D + c * 8;
+        *reinterpret_cast<uint4 *>(p.dk + o) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(p.dv + o) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+
+  if (warp == WARP_MMA) {
+    tmem_alloc(tmem_ptr, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(st_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(done_bar, 1);
+    mbar_init_fence();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == WARP_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      tma_prefetch_desc(&tmdo);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+#pragma unroll
+      for (int h = 0; h < C::NH; ++h) {
+        tma_load_3d(smem + C::OFF_K + h * HALF, &tmk, kv_full, h * 64, kj0, bkv);
+        tma_load_3d(smem + C::OFF_V + h * HALF, &tmv, kv_full, h * 64, kj0, bkv);
+      }
+      int issued = 0;
+      for (int it = 0; it < nitems; ++it) {
+        const int slot = it % NS;
+        if (it >= NS && !mbar_wait(&q_empty[slot], ((it / NS) - 1) & 1, p.timeout_ns, p.err)) break;
+        const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
+        mbar_arrive_expect_tx(&q_full[slot], 2 * C::TILE);
+#pragma unroll
+        for (int h = 0; h < C::NH; ++h) {
+          tma_load_3d(smem + C::OFF_Q + slot * C::TILE + h * HALF, &tmq, &q_full[slot], h * 64, q0,
+                      b * p.Hq + hq);
+          tma_load_3d(smem + C::OFF_DO + slot * C::TILE + h * HALF, &tmdo, &q_full[slot], h * 64, q0,
+                      b * p.Hq + hq);
+        }
+        issued = it + 1;
+      }
+      mbar_wait(kv_full, 0, p.timeout_ns, p.err);
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        mbar_wait(&q_full[t % NS], (t / NS) & 1, p.timeout_ns, p.err);
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V),
+                     qs = smem_u32(smem + C::OFF_Q), dos = smem_u32(smem + C::OFF_DO),
+                     dss = smem_u32(smem + C::OFF_DS);
+      bool ok = mbar_wait(kv_full, 0, p.timeout_ns, p.err);
+      for (int it = 0; ok && it < nitems; ++it) {
+        const int slot = it % NS;
+        if (!mbar_wait(&q_full[slot], (it / NS) & 1, p.timeout_ns, p.err)) break;
+        // TMEM [0,128) still holds the previous dQ until the dQ warps have read it
+        if (it > 0 && !mbar_wait(dq_free, (it - 1) & 1, p.timeout_ns, p.err)) break;
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T: K-major operands, 32 bytes of D per instruction
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
+          mma_ss(tmem + COL_ST, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + slot * C::TILE + o, 16, 1024),
+                 C::IDESC_SS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
+          mma_ss(tmem + COL_DPT, sdesc_sw128(vs + o, 16, 1024), sdesc_sw128(dos + slot * C::TILE + o, 16, 1024),
+                 C::IDESC_SS, kk > 0);
+        }
+        tc_commit(st_full);
+        if (!mbar_wait(p_ready, it & 1, p.timeout_ns, p.err)) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q: A from TMEM (16 queries = 8 columns per
+        // instruction), B = dO / Q MN-major (rows = queries)
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ts(tmem + COL_DV, tmem + COL_ST + kk * 8,
+                 sdesc_sw128(dos + slot * C::TILE + kk * 16 * 128, HALF, 1024), C::IDESC_TS, (it > 0 || kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ts(tmem + COL_DK, tmem + COL_DPT + kk * 8,
+                 sdesc_sw128(qs + slot * C::TILE + kk * 16 * 128, HALF, 1024), C::IDESC_TS, (it > 0 || kk > 0));
+        // dQ = dS K: A = dS (staged as dS^T rows = keys: MN-major), B = K MN-major
+        // (rows = keys); 16 keys per instruction
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tmem + COL_ST, sdesc_sw128(dss + kk * 16 * 128, HALF, 1024),
+                 sdesc_sw128(ks + kk * 16 * 128, HALF, 1024), C::IDESC_DQ, kk > 0);
+        tc_commit(dq_full);
+        tc_commit(&q_empty[slot]);
+      }
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, p.timeout_ns, p.err);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------ gradient warps
+    const int k = warp * 32 + lane;  // key within the tile = TMEM lane
+    const int key = kj0 + k;
+    const uint32_t taddr = tmem + ((warp * 32) << 16);
+    uint8_t *ds_stage = smem + C::OFF_DS;
+    bool ok = true;
+    for (int it = 0; it < nitems; ++it) {
+      const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
+      const size_t rowbase = ((size_t)b * p.Hq + hq) * p.Sq;
+      if (!__all_sync(0xffffffffu, mbar_wait(st_full, it & 1, p.timeout_ns, p.err))) {
+        ok = false;
+        break;
+      }
+      // the staging buffer is free once the previous dQ MMA has read it
+      if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, p.timeout_ns, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BM / 32; ++c) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(taddr + COL_ST + c * 32, sv);
+        tmem_ld32(taddr + COL_DPT + c * 32, dpv);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int q = q0 + c * 32 + e + u;
+            const bool vis = key < p.Sk && q < p.Sq && (!p.causal || key <= q + off);
+            const float l = vis ? __ldg(&p.lse[rowbase + q]) : 0.f;
+            const float dvq = vis ? __ldg(&p.dvec[rowbase + q]) : 0.f;
+            const float pr = (vis && l != -CUDART_INF_F)
+                                 ? fast_exp2(__uint_as_float(sv[e + u]) * p.scale_log2 - l * 1.4426950408889634f)
+                                 : 0.f;
+            pv[u] = pr;
+            dsv[u] = pr * (__uint_as_float(dpv[e + u]) - dvq);
+          }
+          pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(taddr + COL_ST + c * 16, pp);
+        tmem_st16(taddr + COL_DPT + c * 16, dd);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)  // queries c*32 + 8u .. +7
+          *reinterpret_cast<uint4 *>(ds_stage + ds_off(k, c * 4 + u)) =
+              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // dS^T stores before the tensor core reads them
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+    // ---------------------------------------------------- dK, dV epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (nitems - 1) & 1, p.timeout_ns, p.err));
+    if (ok) {
+      tc_fence_after();
+      const size_t o = ((size_t)bkv * p.Sk + min(key, p.Sk - 1)) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32], bv[32];
+        tmem_ld32(taddr + COL_DK + c * 32, a);
+        tmem_ld32(taddr + COL_DV + c * 32, bv);
+        uint32_t pk[16], pv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+          pv[e] = pack_bf16x2(__uint_as_float(bv[2 * e]), __uint_as_float(bv[2 * e + 1]));
+        }
+        if (key < p.Sk) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            reinterpret_cast<uint4 *>(p.dk + o)[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            reinterpret_cast<uint4 *>(p.dv + o)[c * 4 + e] = make_uint4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warps
+    const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
+    const uint32_t taddr = tmem + (((warp & 3) * 32) << 16);
+    for (int it = 0; it < nitems; ++it) {
+      const int hq = kvh * p.g + it / nvis, q = (qt0 + it % nvis) * BM + r;
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, p.timeout_ns, p.err))) break;
+      tc_fence_after();
+      float4 *dst = reinterpret_cast<float4 *>(p.dq_acc + (((size_t)b * p.Hq + hq) * p.Sq + min(q, p.Sq - 1)) * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + COL_ST + c * 32, v);
+        if (q < p.Sq) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicAdd(dst + c * 8 + e,
+                      make_float4(__uint_as_float(v[4 * e]) * p.scale, __uint_as_float(v[4 * e + 1]) * p.scale,
+                                  __uint_as_float(v[4 * e + 2]) * p.scale, __uint_as_float(v[4 * e + 3]) * p.scale));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Dvec = rowsum(dO o O) per query row; zero the dQ accumulator.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                      const __nv_bfloat16 *__restrict__ dout,
+                                                      float *__restrict__ dvec, float *__restrict__ dq_acc,
+                                                      long rows) {
+  const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float acc = 0.f;
+  for (int d = lane * 2; d < D; d += 64) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + row * D + d));
+    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(dout + row * D + d));
+    acc += a.x * c.x + a.y * c.y;
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) dvec[row] = acc;
+  for (int d = lane * 4; d < D; d += 128) *reinterpret_cast<float4 *>(dq_acc + row * D + d) = make_float4(0, 0, 0, 0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
+                                                       long n4) {
+  const long i = (long)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = reinterpret_cast<const float4 *>(dq_acc)[i];
+  uint2 w;
+  w.x = pack_bf16x2(v.x, v.y);
+  w.y = pack_bf16x2(v.z, v.w);
+  reinterpret_cast<uint2 *>(dq)[i] = w;
+}
+
+template <int D>
+cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                   const CUtensorMap &tdo, cudaStream_t st) {
+  using C = Cfg<D>;
+  const long rows = (long)a.B * a.Hq * a.Sq;
+  bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.o),
+                                                                  static_cast<const __nv_bfloat16 *>(a.dout),
+                                                                  a.dvec, a.dq_acc, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  Params p;
+  p.lse = a.lse;
+  p.dvec = a.dvec;
+  p.dq_acc = a.dq_acc;
+  p.dk = static_cast<__nv_bfloat16 *>(a.dk);
+  p.dv = static_cast<__nv_bfloat16 *>(a.dv);
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.causal = a.causal;
+  p.g = a.Hq / a.Hkv;
+  p.nqt = (a.Sq + BM - 1) / BM;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.timeout_ns = a.timeout_ns;
+  p.err = a.err;
+  if ((long)a.B * a.Hkv > 65535) return cudaErrorNotSupported;
+  e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.Sk + BN - 1) / BN), (unsigned)(a.B * a.Hkv));
+  bwd_kernel<D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long n4 = rows * D / 4;
+  bwd_post_kernel<D><<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(a.dq_acc, static_cast<__nv_bfloat16 *>(a.dq), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, cudaStream_t stream) {
+  if (a.D == 128) return bwd::launch<128>(a, tq, tk, tv, tdo, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

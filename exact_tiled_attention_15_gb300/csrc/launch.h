@@ -60,6 +60,23 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tmap_q, const C
 cudaError_t launch_fwd_fp8(const FwdArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
                            const CUtensorMap &tmap_v, cudaStream_t stream);
 
+struct BwdArgs {
+  const void *o, *dout;  // bf16 [B, Hq, Sq, D]
+  const float *lse;      // [B, Hq, Sq]
+  void *dq, *dk, *dv;    // bf16 outputs
+  float *dq_acc;         // workspace [B, Hq, Sq, D] fp32
+  float *dvec;           // workspace [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Sk, D, causal;
+  float scale;
+  uint64_t timeout_ns;
+  unsigned *err;
+};
+
+// Backward: Dvec + zero accumulator, main kernel, dQ conversion.  tq/tk/tv/tdo:
+// 3-D tensor maps (D, S, B*H) with 64 x 128 boxes, 128-byte swizzle.
+cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, cudaStream_t stream);
+
 // Hadamard rotation (signs != nullptr) + per-128x128-tile e4m3 quantisation of a
 // bf16 [B, H, S, 128] tensor.
 cudaError_t launch_rotate_quantize(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,

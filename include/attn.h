@@ -69,6 +69,27 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                      float scale, attn_stream_t stream);
 
+/* attn_bwd_workspace_bytes -- scratch for attn_bwd (fp32 dQ accumulator and
+ * rowsum(dO o O)); 0 on invalid sizes. */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
+
+/*
+ * attn_bwd -- gradients of attn_fwd with recomputation ("Fast Inference and
+ * Training at Scale" §6.21, Idea 2; "Week 13. GPUs and FlashAttention"
+ * step 2: only O and the log-sum-exp are kept from the forward).
+ *   q, k, v, o as for attn_fwd; lse [B, Hq, Sq] fp32 from attn_fwd;
+ *   dout [B, Hq, Sq, D] bf16 (gradient of O).
+ *   dq [B, Hq, Sq, D], dk/dv [B, Hkv, Sk, D] bf16 (written).  With GQA the
+ *   gradient of a key/value head sums over its group's query heads.
+ *   workspace >= attn_bwd_workspace_bytes(B, Hq, Sq, D), 256-byte aligned.
+ *   D == 128 only.  causal, scale as for attn_fwd.
+ * dS and P enter the tensor-core products as bf16; dQ is accumulated in fp32.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                     const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Sq, int Sk,
+                     int D, int causal, float scale, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream);
+
 /*
  * attn_decode_workspace_bytes -- size in bytes of the scratch attn_decode needs
  * for these sizes (partial outputs of the key splits).  0 on invalid sizes.

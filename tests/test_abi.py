@@ -131,3 +131,18 @@ def test_decode_paged_validation(lib):
     assert dec(wsb=n - 1) == INVALID
     assert dec(ps=48, mb=20, wsb=lib.attn_decode_workspace_bytes(4, 8, 2, 48 * 20, 128)) == UNSUPPORTED
     assert dec(D=80, wsb=lib.attn_decode_workspace_bytes(4, 8, 2, 1024, 80)) == UNSUPPORTED
+
+
+def test_bwd_validation(lib):
+    n = lib.attn_bwd_workspace_bytes(1, 2, 128, 128)
+    assert n > 0 and lib.attn_bwd_workspace_bytes(0, 2, 128, 128) == 0
+
+    def bwd(lse=A, ws=A, wsb=n, D=128, Hkv=2):
+        return lib.attn_bwd(p(A), p(A), p(A), p(A), p(lse), p(A), p(A), p(A), p(A), 1, 2, Hkv, 128, 128, D, 1, 0.1,
+                            p(ws), wsb, None)
+
+    assert bwd(lse=0) == INVALID
+    assert bwd(ws=A + 64) == INVALID
+    assert bwd(wsb=n - 1) == INVALID
+    assert bwd(Hkv=3) == INVALID
+    assert bwd(D=64, wsb=lib.attn_bwd_workspace_bytes(1, 2, 128, 64)) == UNSUPPORTED
