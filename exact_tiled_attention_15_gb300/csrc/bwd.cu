@@ -255,6 +255,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < BM / 32; ++c) {
+        // lane l fetches query c*32 + l's LSE (as log2) and Dvec; shuffled below
+        const int ql = q0 + c * 32 + lane;
+        float l2_l = -CUDART_INF_F, dv_l = 0.f;
+        if (ql < p.Sq) {
+          l2_l = __ldg(&p.lse[rowbase + ql]) * 1.4426950408889634f;
+          dv_l = __ldg(&p.dvec[rowbase + ql]);
+        }
         uint32_t sv[32], dpv[32];
         tmem_ld32(taddr + COL_ST + c * 32, sv);
         tmem_ld32(taddr + COL_DPT + c * 32, dpv);
@@ -265,12 +272,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int q = q0 + c * 32 + e + u;
-            const bool vis = key < p.Sk && q < p.Sq && (!p.causal || key <= q + off);
-            const float l = vis ? __ldg(&p.lse[rowbase + q]) : 0.f;
-            const float dvq = vis ? __ldg(&p.dvec[rowbase + q]) : 0.f;
-            const float pr = (vis && l != -CUDART_INF_F)
-                                 ? fast_exp2(__uint_as_float(sv[e + u]) * p.scale_log2 - l * 1.4426950408889634f)
-                                 : 0.f;
+            const float l2 = __shfl_sync(0xffffffffu, l2_l, e + u);
+            const float dvq = __shfl_sync(0xffffffffu, dv_l, e + u);
+            // visible: inside both sequences, under the mask, and the row has a key at all
+            const bool vis = key < p.Sk && q < p.Sq && (!p.causal || key <= q + off) && l2 != -CUDART_INF_F;
+            const float pr = vis ? fast_exp2(__uint_as_float(sv[e + u]) * p.scale_log2 - l2) : 0.f;
             pv[u] = pr;
             dsv[u] = pr * (__uint_as_float(dpv[e + u]) - dvq);
           }
@@ -322,21 +328,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int hq = kvh * p.g + it / nvis, q = (qt0 + it % nvis) * BM + r;
       if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, p.timeout_ns, p.err))) break;
       tc_fence_after();
-      float4 *dst = reinterpret_cast<float4 *>(p.dq_acc + (((size_t)b * p.Hq + hq) * p.Sq + min(q, p.Sq - 1)) * D);
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(taddr + COL_ST + c * 32, v);
-        if (q < p.Sq) {
+      // take the whole row out of TMEM first, so the next tile's MMAs can start
+      uint32_t v[D];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            atomicAdd(dst + c * 8 + e,
-                      make_float4(__uint_as_float(v[4 * e]) * p.scale, __uint_as_float(v[4 * e + 1]) * p.scale,
-                                  __uint_as_float(v[4 * e + 2]) * p.scale, __uint_as_float(v[4 * e + 3]) * p.scale));
-        }
-      }
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(taddr + COL_ST + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
       tc_fence_before();
       mbar_arrive(dq_free);
+      if (q < p.Sq) {
+        float *dst = p.dq_acc + (((size_t)b * p.Hq + hq) * p.Sq + q) * D;
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e)
+          red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]) * p.scale, __uint_as_float(v[4 * e + 1]) * p.scale,
+                     __uint_as_float(v[4 * e + 2]) * p.scale, __uint_as_float(v[4 * e + 3]) * p.scale);
+      }
     }
   }
 
