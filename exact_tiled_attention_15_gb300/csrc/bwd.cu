@@ -239,6 +239,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int key = kj0 + k;
     const uint32_t taddr = tmem + ((warp * 32) << 16);
     uint8_t *ds_stage = smem + C::OFF_DS;
+    // queries this key is visible to: qlo <= q < qhi (causal: q >= key - off;
+    // a key past the end is visible to none)
+    const long long qlo = p.causal ? (long long)key - off : -1;
+    const long long qhi = key < p.Sk ? p.Sq : -1;
     bool ok = true;
     for (int it = 0; it < nitems; ++it) {
       const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
@@ -255,9 +259,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < BM / 32; ++c) {
-        // lane l fetches query c*32 + l's LSE (as log2) and Dvec; shuffled below
-        const int ql = q0 + c * 32 + lane;
-        float l2_l = -CUDART_INF_F, dv_l = 0.f;
+        const int qc = q0 + c * 32;
+        // element e of this chunk (query qc + e) is visible iff elo <= e < ehi
+        const int elo = (int)max(-1LL, min(33LL, qlo - qc));
+        const int ehi = (int)max(-1LL, min(33LL, qhi - qc));
+        // lane l fetches query qc + l's LSE (as log2) and Dvec; shuffled below
+        const int ql = qc + lane;
+        float l2_l = 0.f, dv_l = 0.f;  // (masked below)
         if (ql < p.Sq) {
           l2_l = __ldg(&p.lse[rowbase + ql]) * 1.4426950408889634f;
           dv_l = __ldg(&p.dvec[rowbase + ql]);
@@ -271,12 +279,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           float pv[2], dsv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int q = q0 + c * 32 + e + u;
             const float l2 = __shfl_sync(0xffffffffu, l2_l, e + u);
             const float dvq = __shfl_sync(0xffffffffu, dv_l, e + u);
-            // visible: inside both sequences, under the mask, and the row has a key at all
-            const bool vis = key < p.Sk && q < p.Sq && (!p.causal || key <= q + off) && l2 != -CUDART_INF_F;
-            const float pr = vis ? fast_exp2(__uint_as_float(sv[e + u]) * p.scale_log2 - l2) : 0.f;
+            // a row without any visible key (LSE = -inf) is masked here too,
+            // so the exp2 of +inf it may produce is never selected
+            const float ex = fast_exp2(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -l2));
+            const float pr = (e + u >= elo && e + u < ehi) ? ex : 0.f;
             pv[u] = pr;
             dsv[u] = pr * (__uint_as_float(dpv[e + u]) - dvq);
           }
