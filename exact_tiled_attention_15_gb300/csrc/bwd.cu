@@ -18,15 +18,18 @@
 //                 dV += P^T dO_i and dK += dS^T Q_i (P^T, dS^T read from TMEM,
 //                 accumulators stay in TMEM for the whole CTA);
 //                 dQ_i = dS K_j (dS staged in shared memory, MN-major);
-//   warps 0-3   one thread per key: P^T = exp2(S^T scale log2e - LSE log2e),
+//   warps 0-7   one thread per (key, half of the query tile): stage the
+//               tile's LSE and Dvec in shared memory, then
+//               P^T = exp2(S^T scale log2e - LSE log2e),
 //               dS^T = P^T o (dP^T - Dvec), written back to TMEM (bf16) and
-//               dS^T to shared memory;
-//   warps 4-7   one thread per query row: read dQ_i from TMEM and add
-//               scale * dQ_i into the fp32 accumulator (vector atomics);
+//               dS^T to shared memory; once dQ_i is in TMEM, one thread per
+//               (query row, half of D) adds scale * dQ_i into the fp32
+//               accumulator (vector reductions);
 // then dK (times scale) and dV are written once as bf16.
 // Kernel 3 (bwd_post_kernel): dQ = bf16(accumulator).
-// TMEM columns: S^T [0,128) (then P^T bf16 in [0,64), then dQ_i [0,128)),
-// dP^T [128,256) (then dS^T bf16 in [128,192)), dV [256,384), dK [384,512).
+// TMEM columns: S^T [0,128) (then P^T bf16 in [0,32) and [64,96), then
+// dQ_i [0,128)), dP^T [128,256) (then dS^T bf16 likewise), dV [256,384),
+// dK [384,512).
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -54,7 +57,8 @@ struct Cfg {
   static constexpr int OFF_Q = OFF_V + TILE;        // NS stages of Q
   static constexpr int OFF_DO = OFF_Q + NS * TILE;  // NS stages of dO
   static constexpr int OFF_DS = OFF_DO + NS * TILE; // dS^T staging: 128 keys x 128 queries bf16
-  static constexpr int OFF_BAR = OFF_DS + 2 * HALF;
+  static constexpr int OFF_LSE = OFF_DS + 2 * HALF;  // 128 x (LSE log2, Dvec) of the current item
+  static constexpr int OFF_BAR = OFF_LSE + 128 * 2 * 4;
   static constexpr int NBAR = 1 + 2 * NS + 5;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
@@ -86,6 +90,39 @@ struct Params {
 __device__ __forceinline__ uint32_t ds_off(int k, int c) {
   return (c >> 3) * HALF + k * 128 + (((c & 7) ^ (k & 7)) << 4);
 }
+
+// P^T and dS^T of one key row over 32 queries: from S^T (raw scores) and dP^T
+// in fp32, the per-query LSE (log2 units) and Dvec in shared memory, to packed
+// bf16 pairs.  Element e is visible iff elo <= e < ehi (MASK only); a row
+// without any visible key (LSE = -inf) is always masked, so the exp2 of +inf
+// it may produce is never selected.
+template <bool MASK>
+__device__ __forceinline__ void grad_chunk(const uint32_t (&sv)[32], const uint32_t (&dpv)[32],
+                                           const float4 *l2v, const float4 *dvv, float scale_log2, int elo,
+                                           int ehi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 l4 = l2v[e / 4], d4 = dvv[e / 4];  // broadcast reads
+    const float l2[4] = {l4.x, l4.y, l4.z, l4.w}, dq[4] = {d4.x, d4.y, d4.z, d4.w};
+    float pv[4], dsv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float pr = fast_exp2(fmaf(__uint_as_float(sv[e + u]), scale_log2, -l2[u]));
+      if (MASK) pr = (e + u >= elo && e + u < ehi) ? pr : 0.f;
+      pv[u] = pr;
+      dsv[u] = pr * (__uint_as_float(dpv[e + u]) - dq[u]);
+    }
+    pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+    pp[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+    dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+    dd[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+  }
+}
+
+// TMEM column (relative to S^T or dP^T) of the bf16 P^T / dS^T values of
+// 32-query chunk c: chunks 0, 1 over fp32 chunk 0, chunks 2, 3 over fp32
+// chunk 2, so each half of the warps overwrites only columns it has read.
+__device__ __forceinline__ constexpr uint32_t pcol(int c) { return (c >> 1) * 64 + (c & 1) * 16; }
 
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -139,9 +176,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&q_empty[s], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, 256);
     mbar_init(done_bar, 1);
     mbar_init_fence();
   }
@@ -192,7 +229,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int it = 0; ok && it < nitems; ++it) {
         const int slot = it % NS;
         if (!mbar_wait(&q_full[slot], (it / NS) & 1, p.timeout_ns, p.err)) break;
-        // TMEM [0,128) still holds the previous dQ until the dQ warps have read it
+        // TMEM [0,128) still holds the previous dQ until the compute warps have read it
         if (it > 0 && !mbar_wait(dq_free, (it - 1) & 1, p.timeout_ns, p.err)) break;
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T: K-major operands, 32 bytes of D per instruction
@@ -215,11 +252,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // instruction), B = dO / Q MN-major (rows = queries)
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tmem + COL_DV, tmem + COL_ST + kk * 8,
+          mma_ts(tmem + COL_DV, tmem + COL_ST + pcol(kk >> 1) + (kk & 1) * 8,
                  sdesc_sw128(dos + slot * C::TILE + kk * 16 * 128, HALF, 1024), C::IDESC_TS, (it > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tmem + COL_DK, tmem + COL_DPT + kk * 8,
+          mma_ts(tmem + COL_DK, tmem + COL_DPT + pcol(kk >> 1) + (kk & 1) * 8,
                  sdesc_sw128(qs + slot * C::TILE + kk * 16 * 128, HALF, 1024), C::IDESC_TS, (it > 0 || kk > 0));
         // dQ = dS K: A = dS (staged as dS^T rows = keys: MN-major), B = K MN-major
         // (rows = keys); 16 keys per instruction
@@ -233,66 +270,64 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, p.timeout_ns, p.err);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------ gradient warps
-    const int k = warp * 32 + lane;  // key within the tile = TMEM lane
+  } else {
+    // ------------------------------------------------------- compute warps
+    // Warp w reads TMEM lanes 32*(w%4) .. +31 and takes one half of the
+    // columns: the queries half*64 .. +63 of S^T / dP^T, then the dQ (or dK,
+    // dV) columns half*D/2 .. +D/2-1.
+    const int quad = warp & 3, half = warp >> 2;
+    const int k = quad * 32 + lane;  // key within the tile (S^T, dP^T, dK, dV rows); query row of dQ
     const int key = kj0 + k;
-    const uint32_t taddr = tmem + ((warp * 32) << 16);
+    const uint32_t taddr = tmem + ((quad * 32) << 16);
     uint8_t *ds_stage = smem + C::OFF_DS;
+    float *s_l2 = reinterpret_cast<float *>(smem + C::OFF_LSE), *s_dv = s_l2 + BM;
     // queries this key is visible to: qlo <= q < qhi (causal: q >= key - off;
     // a key past the end is visible to none)
     const long long qlo = p.causal ? (long long)key - off : -1;
     const long long qhi = key < p.Sk ? p.Sq : -1;
+    // this thread's share of an item's per-query values: half 0 the LSE (as
+    // log2), half 1 Dvec, for query q0 + k.  Loaded one item ahead, before the
+    // dQ reductions that would otherwise queue in front of it.
+    auto item_value = [&](int i) -> float {
+      const int hq = kvh * p.g + i / nvis, qt = (qt0 + i % nvis) * BM + k;
+      if (qt >= p.Sq) return 0.f;
+      const size_t r = ((size_t)b * p.Hq + hq) * p.Sq + qt;
+      return half ? __ldg(&p.dvec[r]) : __ldg(&p.lse[r]) * 1.4426950408889634f;
+    };
+    float nval = item_value(0);
     bool ok = true;
     for (int it = 0; it < nitems; ++it) {
       const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
       const size_t rowbase = ((size_t)b * p.Hq + hq) * p.Sq;
-      if (!__all_sync(0xffffffffu, mbar_wait(st_full, it & 1, p.timeout_ns, p.err))) {
-        ok = false;
-        break;
-      }
-      // the staging buffer is free once the previous dQ MMA has read it
-      if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, p.timeout_ns, p.err))) {
+      named_barrier_sync(1, 256);  // every compute thread is done with the previous item's values
+      (half ? s_dv : s_l2)[k] = nval;
+      // st_full also orders this item after the previous dQ MMA (a commit
+      // covers every earlier MMA), the last reader of the dS^T staging buffer;
+      // the barrier publishes the staged values
+      if (!named_barrier_and(1, 256, mbar_wait(st_full, it & 1, p.timeout_ns, p.err))) {
         ok = false;
         break;
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BM / 32; ++c) {
+      for (int c = half * 2; c < half * 2 + 2; ++c) {
         const int qc = q0 + c * 32;
         // element e of this chunk (query qc + e) is visible iff elo <= e < ehi
         const int elo = (int)max(-1LL, min(33LL, qlo - qc));
         const int ehi = (int)max(-1LL, min(33LL, qhi - qc));
-        // lane l fetches query qc + l's LSE (as log2) and Dvec; shuffled below
-        const int ql = qc + lane;
-        float l2_l = 0.f, dv_l = 0.f;  // (masked below)
-        if (ql < p.Sq) {
-          l2_l = __ldg(&p.lse[rowbase + ql]) * 1.4426950408889634f;
-          dv_l = __ldg(&p.dvec[rowbase + ql]);
-        }
+        const float4 *l2v = reinterpret_cast<const float4 *>(s_l2 + c * 32);
+        const float4 *dvv = reinterpret_cast<const float4 *>(s_dv + c * 32);
         uint32_t sv[32], dpv[32];
         tmem_ld32(taddr + COL_ST + c * 32, sv);
         tmem_ld32(taddr + COL_DPT + c * 32, dpv);
         uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float l2 = __shfl_sync(0xffffffffu, l2_l, e + u);
-            const float dvq = __shfl_sync(0xffffffffu, dv_l, e + u);
-            // a row without any visible key (LSE = -inf) is masked here too,
-            // so the exp2 of +inf it may produce is never selected
-            const float ex = fast_exp2(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -l2));
-            const float pr = (e + u >= elo && e + u < ehi) ? ex : 0.f;
-            pv[u] = pr;
-            dsv[u] = pr * (__uint_as_float(dpv[e + u]) - dvq);
-          }
-          pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
-        }
-        tmem_st16(taddr + COL_ST + c * 16, pp);
-        tmem_st16(taddr + COL_DPT + c * 16, dd);
+        if (__all_sync(0xffffffffu, elo <= 0 && ehi >= 32))  // whole chunk visible to every key of the warp
+          grad_chunk<false>(sv, dpv, l2v, dvv, p.scale_log2, 0, 32, pp, dd);
+        else
+          grad_chunk<true>(sv, dpv, l2v, dvv, p.scale_log2, elo, ehi, pp, dd);
+        // bf16 P^T / dS^T of chunk c go over fp32 columns this warp has already read
+        tmem_st16(taddr + COL_ST + pcol(c), pp);
+        tmem_st16(taddr + COL_DPT + pcol(c), dd);
 #pragma unroll
         for (int u = 0; u < 4; ++u)  // queries c*32 + 8u .. +7
           *reinterpret_cast<uint4 *>(ds_stage + ds_off(k, c * 4 + u)) =
@@ -302,17 +337,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();  // dS^T stores before the tensor core reads them
       tc_fence_before();
       mbar_arrive(p_ready);
+      if (it + 1 < nitems) nval = item_value(it + 1);
+      // ---- dQ_i = dS K is in TMEM [0, D): add scale * dQ_i (this warp's columns) into the accumulator
+      if (!named_barrier_and(1, 256, mbar_wait(dq_full, it & 1, p.timeout_ns, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[D / 2];  // out of TMEM first, so the next item's MMAs can start
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(taddr + COL_ST + half * (D / 2) + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+      tc_fence_before();
+      mbar_arrive(dq_free);
+      if (q0 + k < p.Sq) {
+        float *dst = p.dq_acc + (rowbase + q0 + k) * D + half * (D / 2);
+#pragma unroll
+        for (int e = 0; e < D / 8; ++e)
+          red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]) * p.scale, __uint_as_float(v[4 * e + 1]) * p.scale,
+                     __uint_as_float(v[4 * e + 2]) * p.scale, __uint_as_float(v[4 * e + 3]) * p.scale);
+      }
     }
     // ---------------------------------------------------- dK, dV epilogue
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (nitems - 1) & 1, p.timeout_ns, p.err));
+    // (the last dq_full wait above covered every MMA of the CTA)
     if (ok) {
       tc_fence_after();
-      const size_t o = ((size_t)bkv * p.Sk + min(key, p.Sk - 1)) * D;
+      const size_t o = ((size_t)bkv * p.Sk + min(key, p.Sk - 1)) * D + half * (D / 2);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t col = half * (D / 2) + c * 32;
         uint32_t a[32], bv[32];
-        tmem_ld32(taddr + COL_DK + c * 32, a);
-        tmem_ld32(taddr + COL_DV + c * 32, bv);
+        tmem_ld32(taddr + COL_DK + col, a);
+        tmem_ld32(taddr + COL_DV + col, bv);
         uint32_t pk[16], pv[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -326,28 +382,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             reinterpret_cast<uint4 *>(p.dv + o)[c * 4 + e] = make_uint4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
           }
         }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ dQ warps
-    const int r = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
-    const uint32_t taddr = tmem + (((warp & 3) * 32) << 16);
-    for (int it = 0; it < nitems; ++it) {
-      const int hq = kvh * p.g + it / nvis, q = (qt0 + it % nvis) * BM + r;
-      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, p.timeout_ns, p.err))) break;
-      tc_fence_after();
-      // take the whole row out of TMEM first, so the next tile's MMAs can start
-      uint32_t v[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(taddr + COL_ST + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
-      tc_fence_before();
-      mbar_arrive(dq_free);
-      if (q < p.Sq) {
-        float *dst = p.dq_acc + (((size_t)b * p.Hq + hq) * p.Sq + q) * D;
-#pragma unroll
-        for (int e = 0; e < D / 4; ++e)
-          red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]) * p.scale, __uint_as_float(v[4 * e + 1]) * p.scale,
-                     __uint_as_float(v[4 * e + 2]) * p.scale, __uint_as_float(v[4 * e + 3]) * p.scale);
       }
     }
   }
