@@ -364,6 +364,12 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
       !make_tmap(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sk, (uint64_t)B * Hkv, 64, 128) ||
       !make_tmap(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sk, (uint64_t)B * Hkv, 64, 128))
     return ATTN_ERR_CUDA;
+  const size_t rows = (size_t)B * Hq * Sq;
+  float *dq_acc = static_cast<float *>(workspace);
+  // fp32 dQ accumulator, reduced into by TMA in 128-row x 32-column boxes
+  CUtensorMap tdq;
+  if (!make_tmap(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, Sq, (uint64_t)B * Hq, 32, 128))
+    return ATTN_ERR_CUDA;
   attn::BwdArgs a{};
   a.o = o;
   a.dout = dout;
@@ -371,8 +377,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  const size_t rows = (size_t)B * Hq * Sq;
-  a.dq_acc = static_cast<float *>(workspace);
+  a.dq_acc = dq_acc;
   a.dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) + (rows * D * sizeof(float) + 255) / 256 * 256);
   a.B = B;
   a.Hq = Hq;
@@ -385,7 +390,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   a.timeout_ns = kDefaultTimeoutNs;
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
-  return from_cuda(attn::launch_bwd(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(attn::launch_bwd(a, tq, tk, tv, tdo, tdq, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,

@@ -23,8 +23,9 @@
 //               P^T = exp2(S^T scale log2e - LSE log2e),
 //               dS^T = P^T o (dP^T - Dvec), written back to TMEM (bf16) and
 //               dS^T to shared memory; once dQ_i is in TMEM, one thread per
-//               (query row, half of D) adds scale * dQ_i into the fp32
-//               accumulator (vector reductions);
+//               (query row, half of D) stages scale * dQ_i in shared memory
+//               and one thread adds it into the fp32 accumulator with TMA
+//               reduce-add (full 128-byte lines, no per-thread atomics);
 // then dK (times scale) and dV are written once as bf16.
 // Kernel 3 (bwd_post_kernel): dQ = bf16(accumulator).
 // TMEM columns: S^T [0,128) (then P^T bf16 in [0,32) and [64,96), then
@@ -127,7 +128,8 @@ __device__ __forceinline__ constexpr uint32_t pcol(int c) { return (c >> 1) * 64
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, Params p) {
+               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+               const __grid_constant__ CUtensorMap tmdq, Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -298,7 +300,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int it = 0; it < nitems; ++it) {
       const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
-      const size_t rowbase = ((size_t)b * p.Hq + hq) * p.Sq;
       named_barrier_sync(1, 256);  // every compute thread is done with the previous item's values
       (half ? s_dv : s_l2)[k] = nval;
       // st_full also orders this item after the previous dQ MMA (a commit
@@ -350,14 +351,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(taddr + COL_ST + half * (D / 2) + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
       tc_fence_before();
       mbar_arrive(dq_free);
-      if (q0 + k < p.Sq) {
-        float *dst = p.dq_acc + (rowbase + q0 + k) * D + half * (D / 2);
+      // scale * dQ_i goes into the accumulator by TMA reduce-add, staged in the
+      // dS^T buffer (free again: its MMA has completed) as 128-row x 32-column
+      // fp32 boxes with the 128-byte swizzle, one half of D per round
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (half == h) {
 #pragma unroll
-        for (int e = 0; e < D / 8; ++e)
-          red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]) * p.scale, __uint_as_float(v[4 * e + 1]) * p.scale,
-                     __uint_as_float(v[4 * e + 2]) * p.scale, __uint_as_float(v[4 * e + 3]) * p.scale);
+          for (int bx = 0; bx < D / 64; ++bx)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t *w = v + bx * 32 + 4 * j;
+              *reinterpret_cast<float4 *>(ds_stage + bx * HALF + k * 128 + ((j ^ (k & 7)) << 4)) =
+                  make_float4(__uint_as_float(w[0]) * p.scale, __uint_as_float(w[1]) * p.scale,
+                              __uint_as_float(w[2]) * p.scale, __uint_as_float(w[3]) * p.scale);
+            }
+          fence_proxy_async_smem();
+        }
+        named_barrier_sync(1, 256);
+        if (threadIdx.x == 0) {
+          // rows past Sq fall outside the tensor map and are dropped
+          for (int bx = 0; bx < D / 64; ++bx)
+            tma_reduce_add_3d(&tmdq, ds_stage + bx * HALF, h * (D / 2) + bx * 32, q0, b * p.Hq + hq);
+          bulk_commit_group();
+          bulk_wait_read_all();  // before anyone writes the buffer again
+        }
+        if (h == 0) named_barrier_sync(1, 256);
+        // (after the second round, the next item's first barrier orders the
+        // buffer's reuse after thread 0's wait)
       }
     }
+    if (threadIdx.x == 0) bulk_wait_all();  // the accumulator is complete before the CTA ends
     // ---------------------------------------------------- dK, dV epilogue
     // (the last dq_full wait above covered every MMA of the CTA)
     if (ok) {
@@ -429,7 +453,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float *__restrict__
 
 template <int D>
 cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                   const CUtensorMap &tdo, cudaStream_t st) {
+                   const CUtensorMap &tdo, const CUtensorMap &tdq, cudaStream_t st) {
   using C = Cfg<D>;
   const long rows = (long)a.B * a.Hq * a.Sq;
   bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.o),
@@ -459,7 +483,7 @@ cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.Sk + BN - 1) / BN), (unsigned)(a.B * a.Hkv));
-  bwd_kernel<D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+  bwd_kernel<D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long n4 = rows * D / 4;
@@ -470,8 +494,8 @@ cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
 }  // namespace bwd
 
 cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, cudaStream_t stream) {
-  if (a.D == 128) return bwd::launch<128>(a, tq, tk, tv, tdo, stream);
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, cudaStream_t stream) {
+  if (a.D == 128) return bwd::launch<128>(a, tq, tk, tv, tdo, tdq, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -75,7 +75,7 @@ struct BwdArgs {
 // Backward: Dvec + zero accumulator, main kernel, dQ conversion.  tq/tk/tv/tdo:
 // 3-D tensor maps (D, S, B*H) with 64 x 128 boxes, 128-byte swizzle.
 cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &tdo, cudaStream_t stream);
+                       const CUtensorMap &tdo, const CUtensorMap &tdq, cudaStream_t stream);
 
 // Hadamard rotation (signs != nullptr) + per-128x128-tile e4m3 quantisation of a
 // bf16 [B, H, S, 128] tensor.

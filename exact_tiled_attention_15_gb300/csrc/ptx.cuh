@@ -89,6 +89,21 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, ui
       : "memory");
 }
 
+// Element-wise global += shared for one 3-D box (tile mode; the reduction
+// type is the tensor map's); completes through the bulk-group mechanism.
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, const void *smem_src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk group has completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy accesses (TMA writes into the same buffer).
 __device__ __forceinline__ void fence_proxy_async_smem() {
