@@ -11,7 +11,9 @@
 // dQ accumulator.
 // Kernel 2 (bwd_kernel): one CTA per (128-key tile, KV head, batch) walks
 // every visible 128-row query tile of the KV head's query-head group:
-//   warp 8      TMA: K_j, V_j once; Q_i and dO_i into a 2-stage ring;
+//   warp 8      TMA: K_j, V_j once; Q_i and dO_i into a 2-stage ring; adds
+//               each staged scale * dQ_i into the fp32 accumulator with TMA
+//               reduce-add (full 128-byte lines, no per-thread atomics);
 //   warp 9      one thread issues tcgen05.mma:
 //                 S^T = K_j Q_i^T and dP^T = V_j dO_i^T (shared-memory operands,
 //                 fp32 results in TMEM, one lane per key);
@@ -23,9 +25,8 @@
 //               P^T = exp2(S^T scale log2e - LSE log2e),
 //               dS^T = P^T o (dP^T - Dvec), written back to TMEM (bf16) and
 //               dS^T to shared memory; once dQ_i is in TMEM, one thread per
-//               (query row, half of D) stages scale * dQ_i in shared memory
-//               and one thread adds it into the fp32 accumulator with TMA
-//               reduce-add (full 128-byte lines, no per-thread atomics);
+//               (query row, half of D) stages scale * dQ_i in the item's Q / dO
+//               ring slot, which its MMAs no longer need;
 // then dK (times scale) and dV are written once as bf16.
 // Kernel 3 (bwd_post_kernel): dQ = bf16(accumulator).
 // TMEM columns: S^T [0,128) (then P^T bf16 in [0,32) and [64,96), then
@@ -73,6 +74,12 @@ struct Cfg {
   static constexpr uint32_t IDESC_DQ = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
                                        ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // Box bx (fp32 columns 32bx .. 32bx+31) of a 128-row dQ tile staged in ring
+  // slot `slot`: the first D/64 boxes over the slot's Q tile, the rest over its
+  // dO tile (128 rows x 128 bytes each, 1024-byte aligned).
+  static __device__ __forceinline__ uint8_t *dq_box(uint8_t *smem, int slot, int bx) {
+    return smem + slot * TILE + (bx < NH ? OFF_Q + bx * HALF : OFF_DO + (bx - NH) * HALF);
+  }
 };
 
 struct Params {
@@ -135,8 +142,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *kv_full = bars;
-  uint64_t *q_full = bars + 1, *q_empty = q_full + NS;
-  uint64_t *st_full = q_empty + NS, *p_ready = st_full + 1, *dq_full = p_ready + 1, *dq_free = dq_full + 1;
+  uint64_t *q_full = bars + 1, *dq_staged = q_full + NS;
+  uint64_t *st_full = dq_staged + NS, *p_ready = st_full + 1, *dq_full = p_ready + 1, *dq_free = dq_full + 1;
   uint64_t *done_bar = dq_free + 1;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
+      mbar_init(&dq_staged[s], 256);
     }
     mbar_init(st_full, 1);
     mbar_init(p_ready, 256);
@@ -202,21 +209,40 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(smem + C::OFF_K + h * HALF, &tmk, kv_full, h * 64, kj0, bkv);
         tma_load_3d(smem + C::OFF_V + h * HALF, &tmv, kv_full, h * 64, kj0, bkv);
       }
+      // Item i's Q / dO go into ring slot i % NS.  Once item r's MMAs are done,
+      // the compute warps stage scale * dQ_r (fp32, 4 boxes of 128 rows x 32
+      // columns) in that slot; this thread adds it into the accumulator with
+      // TMA reduce-add and refills the slot with item r + NS only after the
+      // reduce has read it.
       int issued = 0;
-      for (int it = 0; it < nitems; ++it) {
-        const int slot = it % NS;
-        if (it >= NS && !mbar_wait(&q_empty[slot], ((it / NS) - 1) & 1, p.timeout_ns, p.err)) break;
-        const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
-        mbar_arrive_expect_tx(&q_full[slot], 2 * C::TILE);
+      bool ok = true;
+      for (int r = 0; ok && r < nitems; ++r) {
+        for (; issued < nitems && issued < r + NS; ++issued) {
+          const int slot = issued % NS;
+          const int hq = kvh * p.g + issued / nvis, q0 = (qt0 + issued % nvis) * BM;
+          mbar_arrive_expect_tx(&q_full[slot], 2 * C::TILE);
 #pragma unroll
-        for (int h = 0; h < C::NH; ++h) {
-          tma_load_3d(smem + C::OFF_Q + slot * C::TILE + h * HALF, &tmq, &q_full[slot], h * 64, q0,
-                      b * p.Hq + hq);
-          tma_load_3d(smem + C::OFF_DO + slot * C::TILE + h * HALF, &tmdo, &q_full[slot], h * 64, q0,
-                      b * p.Hq + hq);
+          for (int h = 0; h < C::NH; ++h) {
+            tma_load_3d(smem + C::OFF_Q + slot * C::TILE + h * HALF, &tmq, &q_full[slot], h * 64, q0,
+                        b * p.Hq + hq);
+            tma_load_3d(smem + C::OFF_DO + slot * C::TILE + h * HALF, &tmdo, &q_full[slot], h * 64, q0,
+                        b * p.Hq + hq);
+          }
         }
-        issued = it + 1;
+        const int slot = r % NS;
+        if (!mbar_wait(&dq_staged[slot], (r / NS) & 1, p.timeout_ns, p.err)) {
+          ok = false;
+          break;
+        }
+        const int hq = kvh * p.g + r / nvis, q0 = (qt0 + r % nvis) * BM;
+        // rows past Sq fall outside the tensor map and are dropped
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx)
+          tma_reduce_add_3d(&tmdq, C::dq_box(smem, slot, bx), bx * 32, q0, b * p.Hq + hq);
+        bulk_commit_group();
+        bulk_wait_read_all();
       }
+      bulk_wait_all();  // the accumulator is complete before the CTA ends
       mbar_wait(kv_full, 0, p.timeout_ns, p.err);
       for (int t = max(0, issued - NS); t < issued; ++t)
         mbar_wait(&q_full[t % NS], (t / NS) & 1, p.timeout_ns, p.err);
@@ -267,7 +293,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_ss(tmem + COL_ST, sdesc_sw128(dss + kk * 16 * 128, HALF, 1024),
                  sdesc_sw128(ks + kk * 16 * 128, HALF, 1024), C::IDESC_DQ, kk > 0);
         tc_commit(dq_full);
-        tc_commit(&q_empty[slot]);
       }
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, p.timeout_ns, p.err);
@@ -299,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     float nval = item_value(0);
     bool ok = true;
     for (int it = 0; it < nitems; ++it) {
-      const int hq = kvh * p.g + it / nvis, q0 = (qt0 + it % nvis) * BM;
+      const int q0 = (qt0 + it % nvis) * BM;
       named_barrier_sync(1, 256);  // every compute thread is done with the previous item's values
       (half ? s_dv : s_l2)[k] = nval;
       // st_full also orders this item after the previous dQ MMA (a commit
@@ -351,37 +376,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(taddr + COL_ST + half * (D / 2) + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
       tc_fence_before();
       mbar_arrive(dq_free);
-      // scale * dQ_i goes into the accumulator by TMA reduce-add, staged in the
-      // dS^T buffer (free again: its MMA has completed) as 128-row x 32-column
-      // fp32 boxes with the 128-byte swizzle, one half of D per round
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (half == h) {
+      // scale * dQ_i, staged in this item's Q / dO slot (free: its MMAs are
+      // done) as 128-row x 32-column fp32 boxes with the 128-byte swizzle; the
+      // TMA thread adds it into the accumulator
 #pragma unroll
-          for (int bx = 0; bx < D / 64; ++bx)
+      for (int bx = 0; bx < D / 64; ++bx)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t *w = v + bx * 32 + 4 * j;
-              *reinterpret_cast<float4 *>(ds_stage + bx * HALF + k * 128 + ((j ^ (k & 7)) << 4)) =
-                  make_float4(__uint_as_float(w[0]) * p.scale, __uint_as_float(w[1]) * p.scale,
-                              __uint_as_float(w[2]) * p.scale, __uint_as_float(w[3]) * p.scale);
-            }
-          fence_proxy_async_smem();
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t *w = v + bx * 32 + 4 * j;
+          *reinterpret_cast<float4 *>(C::dq_box(smem, it % NS, half * (D / 64) + bx) + k * 128 + ((j ^ (k & 7)) << 4)) =
+              make_float4(__uint_as_float(w[0]) * p.scale, __uint_as_float(w[1]) * p.scale,
+                          __uint_as_float(w[2]) * p.scale, __uint_as_float(w[3]) * p.scale);
         }
-        named_barrier_sync(1, 256);
-        if (threadIdx.x == 0) {
-          // rows past Sq fall outside the tensor map and are dropped
-          for (int bx = 0; bx < D / 64; ++bx)
-            tma_reduce_add_3d(&tmdq, ds_stage + bx * HALF, h * (D / 2) + bx * 32, q0, b * p.Hq + hq);
-          bulk_commit_group();
-          bulk_wait_read_all();  // before anyone writes the buffer again
-        }
-        if (h == 0) named_barrier_sync(1, 256);
-        // (after the second round, the next item's first barrier orders the
-        // buffer's reuse after thread 0's wait)
-      }
+      fence_proxy_async_smem();
+      mbar_arrive(&dq_staged[it % NS]);
     }
-    if (threadIdx.x == 0) bulk_wait_all();  // the accumulator is complete before the CTA ends
     // ---------------------------------------------------- dK, dV epilogue
     // (the last dq_full wait above covered every MMA of the CTA)
     if (ok) {
