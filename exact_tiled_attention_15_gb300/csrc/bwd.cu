@@ -106,11 +106,11 @@ __device__ __forceinline__ uint32_t ds_off(int k, int c) {
 // it may produce is never selected.
 template <bool MASK>
 __device__ __forceinline__ void grad_chunk(const uint32_t (&sv)[32], const uint32_t (&dpv)[32],
-                                           const float4 *l2v, const float4 *dvv, float scale_log2, int elo,
+                                           const float4 (&l2v)[8], const float4 *dvv, float scale_log2, int elo,
                                            int ehi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
 #pragma unroll
   for (int e = 0; e < 32; e += 4) {
-    const float4 l4 = l2v[e / 4], d4 = dvv[e / 4];  // broadcast reads
+    const float4 l4 = l2v[e / 4], d4 = dvv[e / 4];
     const float l2[4] = {l4.x, l4.y, l4.z, l4.w}, dq[4] = {d4.x, d4.y, d4.z, d4.w};
     float pv[4], dsv[4];
 #pragma unroll
@@ -341,7 +341,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // element e of this chunk (query qc + e) is visible iff elo <= e < ehi
         const int elo = (int)max(-1LL, min(33LL, qlo - qc));
         const int ehi = (int)max(-1LL, min(33LL, qhi - qc));
-        const float4 *l2v = reinterpret_cast<const float4 *>(s_l2 + c * 32);
+        // the chunk's 32 LSE values (broadcast reads) are in flight during the
+        // TMEM loads; Dvec is read where it is used
+        float4 l2v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) l2v[i] = reinterpret_cast<const float4 *>(s_l2 + c * 32)[i];
         const float4 *dvv = reinterpret_cast<const float4 *>(s_dv + c * 32);
         uint32_t sv[32], dpv[32];
         tmem_ld32(taddr + COL_ST + c * 32, sv);
