@@ -280,7 +280,9 @@ def run_backward(steps, warmup, flush, peaks):
                    "causal": causal},
         "roofline": {"bound": "tensor", "kernel": "bwd_pre + bwd_kernel<128> + bwd_post", "achieved": ach,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                     "peak_source": peaks["source"] + " bf16 burst", "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst",
+                     "traffic": dram_traffic("bwd_kernel<128>", name + "_backward", source_digest("bwd.cu", "ptx.cuh")),
+                     "traffic_kernel": "bwd_kernel<128>",
                      "algorithmic_flops": flops},
         "gpu_launches": 3 * len(ts),
     }
@@ -388,7 +390,9 @@ def run_decode_multi(steps, warmup, flush, peaks, T=4):
                    "Lmax": cfg["Lmax"], "sum_seqlens": int(sum(seqlens))},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel+decode_combine_kernel (T query tokens)",
                      "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                     "peak_source": peaks["source"] + " HBM copy", "traffic": None, "algorithmic_bytes": nbytes},
+                     "peak_source": peaks["source"] + " HBM copy",
+                     "traffic": dram_traffic("decode_split_kernel", name + f"_T{T}", source_digest("decode.cu", "ptx.cuh")),
+                     "algorithmic_bytes": nbytes},
         "gpu_launches": 2 * len(ts),
     }
 
@@ -424,7 +428,10 @@ def run_quant(steps, warmup, flush, peaks):
         "config": {"workload": "fp8_prefill inputs", "B": B, "H": H, "S": S, "D": D, "tensors": 3},
         "roofline": {"bound": "hbm", "kernel": "rotate_quantize_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " HBM copy",
-                     "traffic": None, "algorithmic_bytes": nbytes},
+                     # per step of three launches, like algorithmic_bytes
+                     "traffic": dram_traffic("rotate_quantize_kernel_x3", "fp8_rotate_quantize",
+                                             source_digest("quant.cu")),
+                     "algorithmic_bytes": nbytes},
         "gpu_launches": 3 * len(ts),
     }
 
