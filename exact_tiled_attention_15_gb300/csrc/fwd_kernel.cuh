@@ -345,10 +345,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) mx4[u] = __uint_as_float(s[u]);
 #pragma unroll
-      for (int e = 4; e < 128; e += 8)
+      for (int e = 4; e + 8 <= 128; e += 8)  // s[4 .. 123], two groups of four per step
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           mx4[u] = fmax3(mx4[u], __uint_as_float(s[e + u]), __uint_as_float(s[e + 4 + u]));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx4[u] = fmaxf(mx4[u], __uint_as_float(s[124 + u]));
       const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
       const float m_new = fmaxf(m_use, mx * cj);
       float alpha = 1.f;
