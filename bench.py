@@ -430,7 +430,7 @@ def run_quant(steps, warmup, flush, peaks):
                      "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " HBM copy",
                      # per step of three launches, like algorithmic_bytes
                      "traffic": dram_traffic("rotate_quantize_kernel_x3", "fp8_rotate_quantize",
-                                             source_digest("quant.cu")),
+                                             source_digest("quant.cu", "ptx.cuh")),
                      "algorithmic_bytes": nbytes},
         "gpu_launches": 3 * len(ts),
     }

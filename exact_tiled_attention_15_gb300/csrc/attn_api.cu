@@ -403,7 +403,13 @@ attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scale
   if (D != 128) return ATTN_ERR_UNSUPPORTED;
   if ((int64_t)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
-  return from_cuda(attn::launch_rotate_quantize(x, codes, scales, signs, B, H, S,
+  CUtensorMap tmx, tmc;
+  if (!make_tmap(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, (uint64_t)B * H, 64, 128) ||
+      !make_tmap(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, S, (uint64_t)B * H, 128, 128))
+    return ATTN_ERR_CUDA;
+  unsigned *err = error_word();
+  if (!err) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_rotate_quantize(tmx, tmc, scales, signs, B, H, S, kDefaultTimeoutNs, err,
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -78,8 +78,9 @@ cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMa
                        const CUtensorMap &tdo, const CUtensorMap &tdq, cudaStream_t stream);
 
 // Hadamard rotation (signs != nullptr) + per-128x128-tile e4m3 quantisation of a
-// bf16 [B, H, S, 128] tensor.
-cudaError_t launch_rotate_quantize(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
-                                   int S, cudaStream_t stream);
+// bf16 [B, H, S, 128] tensor: tmx maps x as [B*H, S, 128] bf16 (64 x 128 boxes),
+// tmc the codes as [B*H, S, 128] uint8 (128 x 128 boxes), both 128-byte swizzled.
+cudaError_t launch_rotate_quantize(const CUtensorMap &tmx, const CUtensorMap &tmc, float *scales, const float *signs,
+                                   int B, int H, int S, uint64_t timeout_ns, unsigned *err, cudaStream_t stream);
 
 }  // namespace attn
