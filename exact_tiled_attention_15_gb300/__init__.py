@@ -3,6 +3,7 @@
     from exact_tiled_attention_15_gb300 import fwd, decode, fwd_fp8
 
 ``fwd``      bf16 prefill (causal or not, MHA/GQA/MQA) -> (O, LSE)
+``fwd_host`` the same on host tensors, copies overlapped with the kernels
 ``bwd``      its gradients (dQ, dK, dV), recomputing P from LSE
 ``decode``   one query token per sequence against a KV cache -> (O, LSE)
 ``decode_paged``  the same against a paged KV cache (block table) -> (O, LSE)
@@ -10,7 +11,7 @@
 ``fwd_fp8``  FP8 e4m3 prefill with one scale per 128x128 tile -> (O, LSE)
 ``rotate_quantize_fp8``  Hadamard rotation + per-tile e4m3 quantisation of its inputs
 
-All three call the C ABI of libattn.so (include/attn.h) on the current CUDA
+All of them call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import AttnError, bwd, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, get_error, lib, rotate_quantize_fp8, version  # noqa: F401
+from ._lib import AttnError, bwd, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, fwd_host, fwd_host_workspace_bytes, get_error, lib, rotate_quantize_fp8, version  # noqa: F401

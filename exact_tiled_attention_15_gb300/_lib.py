@@ -24,6 +24,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3:
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
@@ -111,6 +113,49 @@ def fwd(q, k, v, causal=False, scale=None, return_lse=True, out=None, lse_out=No
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
                         1 if causal else 0, scale, _stream(q.device))
     _check(st, "attn_fwd")
+    return o, lse
+
+
+def _need_host(t, name, dtype, dims):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D) -> int:
+    return int(lib().attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D))
+
+
+def fwd_host(q, k, v, causal=False, scale=None, out=None, lse_out=None, workspace=None, device=None):
+    """fwd on host (CPU, ideally pinned) tensors; copies and kernels overlap in
+    chunks.  Returns (o, lse) as host tensors, valid once the current CUDA
+    stream of ``device`` has been synchronised."""
+    _need_host(q, "q", torch.bfloat16, 4)
+    _need_host(k, "k", torch.bfloat16, 4)
+    _need_host(v, "v", torch.bfloat16, 4)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, Sk, D] matching q")
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    lse = lse_out if lse_out is not None else torch.empty(B, Hq, Sq, dtype=torch.float32, pin_memory=True)
+    _need_host(o, "out", torch.bfloat16, 4)
+    nbytes = fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                             Sq, Sk, D, 1 if causal else 0, scale, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(dev))
+    _check(st, "attn_fwd_host")
     return o, lse
 
 

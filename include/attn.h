@@ -69,6 +69,33 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                      float scale, attn_stream_t stream);
 
+/* attn_fwd_host_workspace_bytes -- device scratch for attn_fwd_host (three
+ * chunk buffers); 0 on invalid sizes. */
+size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D);
+
+/*
+ * attn_fwd_host -- attn_fwd for q, k, v, o (and lse, nullable) in HOST memory,
+ * same layouts and arguments.  The (batch, KV head) units are independent
+ * problems ("Fast Inference and Training at Scale" §6.2: each query head reads
+ * only its group's K and V), so the call is cut into chunks of consecutive
+ * units whose host-to-device copies, kernels and device-to-host copies overlap
+ * on three streams; each chunk is an attn_fwd call, so the results equal
+ * attn_fwd's on device copies of the same data.
+ *   workspace: device memory >= attn_fwd_host_workspace_bytes(...), 256-byte
+ *   aligned, owned by the caller.
+ *   Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ *   the copies to overlap; pageable memory works but serialises them.
+ * Asynchronous: work before the call on `stream` is ordered before it, and
+ * `stream` waits until o and lse are back in host memory; the host must not
+ * read o before synchronising the stream.  On first use per calling thread and
+ * device it creates two CUDA streams and ten events, kept until process exit.
+ * Errors: as attn_fwd; ATTN_ERR_INVALID_ARG for a short or misaligned
+ * workspace.
+ */
+attn_status attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                          void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
 /* attn_bwd_workspace_bytes -- scratch for attn_bwd (fp32 dQ accumulator and
  * rowsum(dO o O)); 0 on invalid sizes. */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D);

@@ -146,3 +146,25 @@ def test_bwd_validation(lib):
     assert bwd(wsb=n - 1) == INVALID
     assert bwd(Hkv=3) == INVALID
     assert bwd(D=64, wsb=lib.attn_bwd_workspace_bytes(1, 2, 128, 64)) == UNSUPPORTED
+
+
+def test_fwd_host_validation(lib):
+    """The host-buffer forward checks its arguments before any CUDA call; its
+    workspace holds three chunk buffers of whole (batch, KV head) units."""
+    n = lib.attn_fwd_host_workspace_bytes(2, 32, 32, 4096, 4096, 128)
+    assert n > 0 and lib.attn_fwd_host_workspace_bytes(2, 32, 3, 4096, 4096, 128) == 0
+    assert lib.attn_fwd_host_workspace_bytes(0, 32, 32, 4096, 4096, 128) == 0
+    # more units never need less scratch, and a unit is at least the bytes of its Q, K, V, O, LSE
+    assert lib.attn_fwd_host_workspace_bytes(4, 32, 32, 4096, 4096, 128) >= n
+    unit = 4096 * 128 * 2 * 4 + 4096 * 4
+    assert n >= 3 * unit
+
+    def host(q=A, ws=A, wsb=n, Hkv=32, D=128):
+        return lib.attn_fwd_host(p(q), p(A), p(A), p(A), p(A), 2, 32, Hkv, 4096, 4096, D, 1, 0.1, p(ws), wsb, None)
+
+    assert host(q=0) == INVALID
+    assert host(ws=0) == INVALID
+    assert host(ws=A + 16) == INVALID
+    assert host(wsb=n - 1) == INVALID
+    assert host(Hkv=3) == INVALID
+    assert host(D=96, wsb=lib.attn_fwd_host_workspace_bytes(2, 32, 32, 4096, 4096, 96)) == UNSUPPORTED
