@@ -10,9 +10,9 @@
  * "Hardware Co-Design" (FlashAttention section, the online-softmax update).
  *
  * Conventions shared by every call
- *   - Pointers are DEVICE pointers owned by the caller; the library keeps no
- *     pointer after a call returns and allocates no device memory (the decode
- *     workspace is passed in).
+ *   - Pointers are DEVICE pointers owned by the caller (attn_fwd_host takes
+ *     its tensors in host memory); the library keeps no pointer after a call
+ *     returns and allocates no device memory (every workspace is passed in).
  *   - Layouts are dense row-major ("contiguous"): Q/O [B, Hq, Sq, D],
  *     K/V [B, Hkv, Sk, D], LSE [B, Hq, Sq].  Every tensor pointer must be
  *     16-byte aligned.
@@ -28,8 +28,10 @@
  *     failure returns ATTN_ERR_CUDA.  Device-side faults of the pipeline (a
  *     bounded wait that ran out) are recorded in a device error word that
  *     attn_get_error() reads.
- *   - The library is stateless apart from that error word and a per-device
- *     cache of kernel attributes; calls may come from several host threads.
+ *   - The library is stateless apart from that error word, a per-device
+ *     cache of kernel attributes and, for attn_fwd_host, two CUDA streams and
+ *     ten events per calling thread and device; calls may come from several
+ *     host threads.
  */
 #ifndef EXACT_TILED_ATTENTION_ATTN_H
 #define EXACT_TILED_ATTENTION_ATTN_H
