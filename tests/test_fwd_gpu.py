@@ -110,3 +110,23 @@ def test_train_prefill_full_size_sampled():
 def test_long_gqa_prefill_full_size_sampled():
     """B=1, 32/8 heads, S=16384, D=128, causal, 1% of K entries x20."""
     _sampled("long_gqa_prefill", 12, [(0, 0), (0, 3), (0, 4), (0, 17), (0, 31)])
+
+
+def test_very_long_sequence_sampled():
+    """A 65,536-token causal GQA prefill (4 query heads on 1 KV head): 256 query
+    blocks per head, 512 key tiles for the last rows; sampled rows against the
+    oracle, including the first and last rows and tile edges."""
+    import exact_tiled_attention_15_gb300 as eta
+    S, D = 65536, 128
+    w = workloads.make_prefill(1, 4, 1, S, S, D, seed=9)
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, k, v, causal=True)
+    assert eta.get_error() == 0
+    o, lse = o.cpu(), lse.cpu()
+    rng = np.random.default_rng(2)
+    for h in (0, 3):
+        rows = np.unique(np.concatenate([[0, 127, 128, 32767, 32768, S - 129, S - 128, S - 1],
+                                         rng.integers(0, S, 8)]))
+        Or, Lr = oracle.attention_rows(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                                       0, h, rows, True, 1.0 / np.sqrt(D))
+        check_bf16(o[0, h, rows].double().numpy(), Or, lse[0, h, rows].numpy(), Lr, what=f"S=65536 h{h}")
