@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--only", choices=["train_prefill_mha", "train_prefill_mha_backward", "long_gqa_prefill",
+    ap.add_argument("--only", choices=["train_prefill_mha", "train_prefill_mha_backward", "long_gqa_prefill", "chunked_prefill",
                                        "gqa_decode", "gqa_decode_paged",
                                        "gqa_decode_T4", "fp8_rotate_quantize", "fp8_prefill"],
                     help="run one workload leg alone and print its figures (for profiling)")
@@ -250,6 +250,39 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
         del ws
     del q, k, v, o, lse
     return res
+
+
+def run_chunked_prefill(steps, warmup, flush, peaks):
+    """A chunk of new queries against a dense KV cache that already holds them
+    (Sq < Sk, causal aligned at the bottom right): attn_fwd with Sq != Sk."""
+    import torch
+    import exact_tiled_attention_15_gb300 as eta
+    from exact_tiled_attention_15_gb300 import accounting as acc, workloads
+    name = "chunked_prefill"
+    cfg = workloads.WORKLOADS[name]
+    B, Hq, Hkv, Sq, Sk, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["Sq"], cfg["Sk"], cfg["D"]
+    w = workloads.make_workload(name, seed=0)
+    dev = torch.device("cuda")
+    q, k, v = (w[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Sq, device=dev, dtype=torch.float32)
+    fn = lambda: eta.fwd(q, k, v, causal=True, out=o, lse_out=lse)  # noqa: E731
+    ts = time_steps(fn, steps, warmup, flush)
+    if eta.get_error() != 0:
+        raise RuntimeError(f"{name}: device-side error")
+    flops = acc.prefill_flops_exact(B, Hq, Sq, Sk, D, True)
+    ms = statistics.mean(ts)
+    ach = flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": "attention TFLOP/s (bf16 chunked prefill against a KV cache, exact visible pairs)",
+        "unit": "TFLOP/s", "value": ach, "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Sk": Sk, "D": D, "causal": True},
+        "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Bf16,128>", "achieved": ach,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                     "peak_source": peaks["source"] + " bf16 burst", "traffic": None,
+                     "algorithmic_flops": flops, "algorithmic_bytes": acc.prefill_bytes(B, Hq, Hkv, Sq, Sk, D)},
+        "gpu_launches": len(ts),
+    }
 
 
 def run_backward(steps, warmup, flush, peaks):
@@ -548,6 +581,8 @@ def main():
     if args.only:
         if args.only == "gqa_decode":
             res = run_decode(args.steps, args.warmup, flush, peaks)
+        elif args.only == "chunked_prefill":
+            res = run_chunked_prefill(args.steps, args.warmup, flush, peaks)
         elif args.only == "train_prefill_mha_backward":
             res = run_backward(args.steps, args.warmup, flush, peaks)
         elif args.only == "gqa_decode_paged":
@@ -577,6 +612,7 @@ def main():
     extras = {}
     if not args.no_extras:
         extras["long_gqa_prefill"] = run_prefill("long_gqa_prefill", max(5, args.steps // 4), args.warmup, flush, peaks)
+        extras["chunked_prefill"] = run_chunked_prefill(args.steps, args.warmup, flush, peaks)
         extras["train_prefill_mha_backward"] = run_backward(max(5, args.steps // 4), args.warmup, flush, peaks)
         extras["gqa_decode"] = run_decode(args.steps, args.warmup, flush, peaks)
         extras["gqa_decode_paged"] = run_decode_paged(args.steps, args.warmup, flush, peaks)

@@ -17,6 +17,20 @@ def prefill_flops(B, Hq, Sq, Sk, D, causal) -> float:
     return f / 2 if causal else f
 
 
+def visible_pairs(Sq, Sk, causal) -> int:
+    """(query, key) pairs under the mask of one head: all Sq * Sk, or with the
+    bottom-right causal alignment, row i sees keys j <= i + Sk - Sq."""
+    if not causal:
+        return Sq * Sk
+    off = Sk - Sq
+    return sum(max(0, min(Sk, i + off + 1)) for i in range(Sq))
+
+
+def prefill_flops_exact(B, Hq, Sq, Sk, D, causal) -> float:
+    """4 * D FLOPs per visible (query, key) pair (Q K^T and P V), counted exactly."""
+    return 4.0 * D * B * Hq * visible_pairs(Sq, Sk, causal)
+
+
 def backward_flops(B, Hq, Sq, Sk, D, causal) -> float:
     """Five products per score (S and dP recomputed, dV, dK, dQ), 2*D FLOPs
     each: 2.5 x the forward's count."""

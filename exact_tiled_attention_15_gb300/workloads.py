@@ -32,6 +32,8 @@ WORKLOADS = {
     "train_prefill_mha": dict(kind="prefill", B=4, Hq=32, Hkv=32, S=4096, D=128, causal=True),
     "long_gqa_prefill": dict(kind="prefill", B=1, Hq=32, Hkv=8, S=16384, D=128, causal=True,
                              k_outlier_frac=0.01, k_outlier_mult=20.0),
+    # a 512-token chunk of new queries against a cache of 8192 keys that already holds them
+    "chunked_prefill": dict(kind="chunked_prefill", B=8, Hq=32, Hkv=8, Sq=512, Sk=8192, D=128, causal=True),
     "gqa_decode": dict(kind="decode", B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192),
     "gqa_decode_paged": dict(kind="paged_decode", B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192, page_size=64),
     "fp8_prefill": dict(kind="fp8", B=2, Hq=16, Hkv=16, S=8192, D=128, causal=False,
@@ -196,6 +198,8 @@ def make_workload(name: str, seed: int = 0, **override):
     if kind == "prefill":
         return make_prefill(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["S"], cfg["D"], seed,
                             cfg.get("k_outlier_frac", 0.0), cfg.get("k_outlier_mult", 1.0))
+    if kind == "chunked_prefill":
+        return make_prefill(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["Sq"], cfg["Sk"], cfg["D"], seed)
     if kind == "decode":
         return make_decode(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Lmin"], cfg["Lmax"], seed)
     if kind == "fp8":

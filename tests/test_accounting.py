@@ -42,3 +42,17 @@ def test_benchmark_workloads():
     assert acc.prefill_flops(4, 32, 4096, 4096, 128, True) == pytest.approx(549.755813888e9)
     # decode, seed-0 lengths sum to 299,418: 1.2264 GB of K and V
     assert acc.decode_kv_bytes([299418], 8, 128) == pytest.approx(1.226416128e9)
+
+
+def test_visible_pairs_exact_count():
+    """Brute force over a small grid; square causal is S(S+1)/2 (the 'halved'
+    count plus the diagonal); Sq > Sk leaves the first rows empty."""
+    import numpy as np
+    from exact_tiled_attention_15_gb300 import accounting as acc
+    for Sq, Sk in ((1, 1), (5, 5), (3, 9), (9, 3), (128, 1000)):
+        rows = np.arange(Sq)[:, None]
+        keys = np.arange(Sk)[None, :]
+        assert acc.visible_pairs(Sq, Sk, True) == int((keys <= rows + (Sk - Sq)).sum())
+        assert acc.visible_pairs(Sq, Sk, False) == Sq * Sk
+    assert acc.visible_pairs(4096, 4096, True) == 4096 * 4097 // 2
+    assert acc.prefill_flops_exact(2, 3, 7, 7, 16, False) == 4 * 16 * 2 * 3 * 49

@@ -130,3 +130,20 @@ def test_very_long_sequence_sampled():
         Or, Lr = oracle.attention_rows(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
                                        0, h, rows, True, 1.0 / np.sqrt(D))
         check_bf16(o[0, h, rows].double().numpy(), Or, lse[0, h, rows].numpy(), Lr, what=f"S=65536 h{h}")
+
+
+def test_chunked_prefill_full_size_sampled():
+    """A 512-token chunk against an 8192-key cache that holds it (B=8, 32/8
+    heads, causal aligned at the bottom right): sampled rows of 4 heads."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_workload("chunked_prefill", seed=0)
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, k, v, causal=True)
+    assert eta.get_error() == 0
+    o, lse = o.cpu(), lse.cpu()
+    rng = np.random.default_rng(4)
+    for (b, h) in ((0, 0), (3, 9), (7, 30), (7, 31)):
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 511], rng.integers(0, 512, 8)]))
+        Or, Lr = oracle.attention_rows(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                                       b, h, rows, True, 1.0 / np.sqrt(128))
+        check_bf16(o[b, h, rows].double().numpy(), Or, lse[b, h, rows].numpy(), Lr, what=f"chunked b{b} h{h}")
