@@ -46,3 +46,23 @@ def test_host_many_chunks(pinned):
     n1 = eta.fwd_host_workspace_bytes(2, 32, 32, 4096, 4096, 128)
     assert n1 < 64 * 3 * 4096 * 128 * 2 * 4  # smaller than staging every unit
     run(2, 32, 32, 4096, 128, True, pinned=pinned, seed=3)
+
+
+def test_host_without_lse_through_the_c_abi():
+    """lse = NULL: the call skips that copy and O is unchanged."""
+    import ctypes
+    import exact_tiled_attention_15_gb300 as eta
+    B, Hq, Hkv, S, D = 1, 8, 2, 700, 128
+    w = workloads.make_prefill(B, Hq, Hkv, S, S, D, seed=12)
+    hq, hk, hv = (w[n].pin_memory() for n in ("q", "k", "v"))
+    o = torch.empty(hq.shape, dtype=hq.dtype, pin_memory=True)
+    nbytes = eta.fwd_host_workspace_bytes(B, Hq, Hkv, S, S, D)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    st = eta.lib().attn_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), o.data_ptr(), None, B, Hq, Hkv, S, S,
+                                 D, 1, 1.0 / np.sqrt(D), ctypes.c_void_p(ws.data_ptr()), nbytes,
+                                 ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize(DEV)
+    assert eta.get_error() == 0
+    o_d, _ = eta.fwd(hq.to(DEV), hk.to(DEV), hv.to(DEV), causal=True)
+    assert torch.equal(o, o_d.cpu())
