@@ -199,6 +199,44 @@ def time_steps(fn, steps, warmup, flush):
 
 
 # ---------------------------------------------------------------- workloads
+# two-sided 95 % Student-t quantiles by degrees of freedom (larger: the normal 1.96)
+_T95 = {1: 12.706, 2: 4.303, 3: 3.182, 4: 2.776, 5: 2.571, 6: 2.447, 7: 2.365, 8: 2.306, 9: 2.262, 10: 2.228,
+        12: 2.179, 15: 2.131, 20: 2.086, 25: 2.060, 30: 2.042, 40: 2.021, 60: 2.000, 120: 1.980}
+
+
+# Nominal dense per-GPU figures of the datasheet, beside the measured peaks the
+# fractions are graded on: bf16 2.25 PFLOP/s, FP8 4.5 PFLOP/s, HBM3e 7.9 TB/s.
+SPEC = {"bf16": 2250.0, "fp8": 4500.0, "hbm": 7900.0}
+
+
+def add_spec(roofline):
+    """Add the fraction of the nominal datasheet peak to a roofline object."""
+    if not roofline or roofline.get("achieved") is None:
+        return roofline
+    if roofline["unit"] == "GB/s":
+        peak = SPEC["hbm"]
+    else:
+        peak = SPEC["fp8"] if "Fp8" in roofline.get("kernel", "") else SPEC["bf16"]
+    roofline["spec_peak"] = peak
+    roofline["frac_of_spec"] = roofline["achieved"] / peak
+    roofline["spec_source"] = "nominal datasheet, dense"
+    return roofline
+
+
+def timing_stats(ts):
+    """Median, 95th percentile and the half-width of the Student-t 95 %
+    confidence interval of the mean, in ms, of per-step times."""
+    n = len(ts)
+    srt = sorted(ts)
+    p95 = srt[min(n - 1, int(round(0.95 * (n - 1))))]
+    ci = None
+    if n > 1:
+        dof = n - 1
+        t = next((v for k, v in sorted(_T95.items()) if k >= dof), 1.96)
+        ci = t * statistics.stdev(ts) / math.sqrt(n)
+    return {"ms_median": statistics.median(ts), "ms_p95": p95, "ms_ci95": ci}
+
+
 def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
     import torch
     import exact_tiled_attention_15_gb300 as eta
@@ -220,7 +258,7 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
     digest = source_digest("fwd_kernel.cuh", "fwd_bf16.cu", "ptx.cuh")
     res = {
         "metric": "attention TFLOP/s (bf16 prefill)", "unit": "TFLOP/s", "value": ach,
-        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Sk": S, "D": D, "causal": causal},
         "flops_per_step": flops,
         "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Bf16,128>", "achieved": ach, "peak": peaks["bf16_tflops"],
@@ -275,7 +313,7 @@ def run_chunked_prefill(steps, warmup, flush, peaks):
     ach = flops / (ms * 1e-3) / 1e12
     return {
         "metric": "attention TFLOP/s (bf16 chunked prefill against a KV cache, exact visible pairs)",
-        "unit": "TFLOP/s", "value": ach, "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "unit": "TFLOP/s", "value": ach, "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Sk": Sk, "D": D, "causal": True},
         "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Bf16,128>", "achieved": ach,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
@@ -310,7 +348,7 @@ def run_backward(steps, warmup, flush, peaks):
     ach = flops / (ms * 1e-3) / 1e12
     return {
         "metric": "attention backward TFLOP/s (bf16, recomputation)", "unit": "TFLOP/s", "value": ach,
-        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name + "_backward", "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Sk": S, "D": D,
                    "causal": causal},
         "roofline": {"bound": "tensor", "kernel": "bwd_pre + bwd_kernel<128> + bwd_post", "achieved": ach,
@@ -347,7 +385,7 @@ def run_decode(steps, warmup, flush, peaks):
     digest = source_digest("decode.cu", "ptx.cuh")
     return {
         "metric": "KV-read GB/s (bf16 GQA decode)", "unit": "GB/s", "value": gbs,
-        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Lmin": cfg["Lmin"],
                    "Lmax": cfg["Lmax"], "sum_seqlens": int(sum(seqlens))},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel+decode_combine_kernel", "achieved": gbs,
@@ -386,7 +424,7 @@ def run_decode_paged(steps, warmup, flush, peaks):
     digest = source_digest("decode.cu", "ptx.cuh")
     return {
         "metric": "KV-read GB/s (bf16 GQA decode, paged KV cache)", "unit": "GB/s", "value": gbs,
-        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Lmin": cfg["Lmin"],
                    "Lmax": cfg["Lmax"], "page_size": ps, "sum_seqlens": int(sum(seqlens))},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,paged>+decode_combine_kernel",
@@ -420,7 +458,7 @@ def run_decode_multi(steps, warmup, flush, peaks, T=4):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {
         "metric": f"KV-read GB/s (bf16 GQA decode, {T} causal query tokens per sequence)", "unit": "GB/s",
-        "value": gbs, "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "value": gbs, "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name + f"_T{T}", "B": B, "Hq": Hq, "Hkv": Hkv, "T": T, "D": D, "Lmin": cfg["Lmin"],
                    "Lmax": cfg["Lmax"], "sum_seqlens": int(sum(seqlens))},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel+decode_combine_kernel (T query tokens)",
@@ -459,7 +497,7 @@ def run_quant(steps, warmup, flush, peaks):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {
         "metric": "GB/s (Hadamard rotate + per-tile e4m3 quantise of Q, K, V)", "unit": "GB/s", "value": gbs,
-        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": "fp8_prefill inputs", "B": B, "H": H, "S": S, "D": D, "tensors": 3},
         "roofline": {"bound": "hbm", "kernel": "rotate_quantize_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"] + " HBM copy",
@@ -493,7 +531,7 @@ def run_fp8(steps, warmup, flush, peaks):
     digest = source_digest("fwd_kernel.cuh", "fwd_fp8.cu", "ptx.cuh")
     return {
         "metric": "attention TFLOP/s (FP8 e4m3 prefill)", "unit": "TFLOP/s", "value": ach,
-        "ms_per_step": ms, "ms_median": statistics.median(ts), "steps": len(ts),
+        "ms_per_step": ms, **timing_stats(ts), "steps": len(ts),
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Sk": S, "D": D, "causal": causal},
         "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Fp8,128>", "achieved": ach, "peak": peak,
                      "unit": "TFLOP/s", "frac": ach / peak,
@@ -596,6 +634,7 @@ def main():
         else:
             res = run_prefill(args.only, args.steps, args.warmup, flush, peaks)
         if rank == 0:
+            add_spec(res.get("roofline"))
             print(json.dumps(dict(res, only=args.only)), flush=True)
         return
     clocks = ClockSampler(local)
@@ -626,11 +665,16 @@ def main():
     clk = clocks.stop()
     if rank != 0:
         return
+    add_spec(head["roofline"])
+    for leg in extras.values():
+        if isinstance(leg, dict) and "roofline" in leg:
+            add_spec(leg["roofline"])
     value = whole_job_tflops(head["flops_per_step"], ws, step_ms)
     line = {
         "metric": HEADLINE_METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": step_ms, "ms_median": head["ms_median"], "ms_p95": head["ms_p95"],
+        "ms_ci95": head["ms_ci95"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": dict(head["config"], l2="flushed between steps (256 MB write outside the timed events); "
                                           "inputs 402 MB also exceed the 129 MB L2",
