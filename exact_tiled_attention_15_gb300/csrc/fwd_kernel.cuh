@@ -245,14 +245,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     // contiguously so its result is ready as early as possible.
     if (lane == 0) {
       const uint32_t qs = smem_u32(smem + C::OFF_Q), ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V);
+      // base descriptors (start address + constant offsets below)
+      const uint64_t dq0 = sdesc_sw128(qs, 16, 1024), dk0 = sdesc_sw128(ks, 16, 1024),
+                     dv0 = sdesc_sw128(vs, HALF, 1024);
       // S_i = Q_i K_j^T: K-major operands, 32 bytes of the head dimension per instruction
       auto issue_s = [&](int i, int j) {
         const int slot = j % NSK;
+        const uint64_t dq = sdesc_add(dq0, i * C::TILE), dk = sdesc_add(dk0, slot * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / T::kMmaK; ++kk) {
           const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_qk<T>(tmem + C::col_s(i), sdesc_sw128(qs + i * C::TILE + o, 16, 1024),
-                    sdesc_sw128(ks + slot * C::TILE + o, 16, 1024), C::IDESC_QK, kk > 0);
+          mma_qk<T>(tmem + C::col_s(i), sdesc_add(dq, o), sdesc_add(dk, o), C::IDESC_QK, kk > 0);
         }
         tc_commit(&s_full[i]);
       };
@@ -262,10 +265,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&p_full[i], j & 1, p.timeout_ns, p.err)) return false;
         tc_fence_after();
         const int slot = j % NSV;
+        const uint64_t dv = sdesc_add(dv0, slot * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < BN / T::kMmaK; ++kk)
-          mma_pv<T>(tmem + C::col_o(i), tmem + C::col_s(i) + kk * 8,
-                    sdesc_sw128(vs + slot * C::TILE + kk * T::kMmaK * 128, HALF, 1024), C::IDESC_PV,
+          mma_pv<T>(tmem + C::col_o(i), tmem + C::col_s(i) + kk * 8, sdesc_add(dv, kk * T::kMmaK * 128), C::IDESC_PV,
                     (j > 0 || kk > 0));
         tc_commit(&o_full[i]);
         return true;

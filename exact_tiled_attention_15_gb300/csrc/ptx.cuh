@@ -247,6 +247,13 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint
 
 // Shared-memory matrix descriptor (tcgen05 form, 128-byte swizzle).
 //   start: shared address of the first 16-byte chunk; lbo/sbo in bytes.
+// A descriptor whose start address is `bytes` (a multiple of 16) further on:
+// the start field is the low 14 bits of the low word, and shared-memory
+// addresses stay below 2^18 bytes, so the add never carries out of it.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return (desc & 0xFFFFFFFF00000000ull) | (uint32_t)((uint32_t)desc + (bytes >> 4));
+}
+
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((start & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) /* descriptor version */ |
