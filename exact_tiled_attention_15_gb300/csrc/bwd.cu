@@ -253,6 +253,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t ks = smem_u32(smem + C::OFF_K), vs = smem_u32(smem + C::OFF_V),
                      qs = smem_u32(smem + C::OFF_Q), dos = smem_u32(smem + C::OFF_DO),
                      dss = smem_u32(smem + C::OFF_DS);
+      // descriptors built once: K-major reads (LBO 16) and MN-major reads (LBO = half tile),
+      // advanced per product by byte offsets
+      const uint64_t k_km = sdesc_sw128(ks, 16, 1024), v_km = sdesc_sw128(vs, 16, 1024),
+                     q_km = sdesc_sw128(qs, 16, 1024), do_km = sdesc_sw128(dos, 16, 1024),
+                     q_mn = sdesc_sw128(qs, HALF, 1024), do_mn = sdesc_sw128(dos, HALF, 1024),
+                     ds_mn = sdesc_sw128(dss, HALF, 1024), k_mn = sdesc_sw128(ks, HALF, 1024);
       bool ok = mbar_wait(kv_full, 0, p.timeout_ns, p.err);
       for (int it = 0; ok && it < nitems; ++it) {
         const int slot = it % NS;
@@ -261,37 +267,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (it > 0 && !mbar_wait(dq_free, (it - 1) & 1, p.timeout_ns, p.err)) break;
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T: K-major operands, 32 bytes of D per instruction
+        const uint32_t so = slot * C::TILE;
+        const uint64_t q_k = sdesc_add(q_km, so), do_k = sdesc_add(do_km, so);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_ss(tmem + COL_ST, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + slot * C::TILE + o, 16, 1024),
-                 C::IDESC_SS, kk > 0);
+          mma_ss(tmem + COL_ST, sdesc_add(k_km, o), sdesc_add(q_k, o), C::IDESC_SS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_ss(tmem + COL_DPT, sdesc_sw128(vs + o, 16, 1024), sdesc_sw128(dos + slot * C::TILE + o, 16, 1024),
-                 C::IDESC_SS, kk > 0);
+          mma_ss(tmem + COL_DPT, sdesc_add(v_km, o), sdesc_add(do_k, o), C::IDESC_SS, kk > 0);
         }
         tc_commit(st_full);
         if (!mbar_wait(p_ready, it & 1, p.timeout_ns, p.err)) break;
         tc_fence_after();
         // dV += P^T dO and dK += dS^T Q: A from TMEM (16 queries = 8 columns per
         // instruction), B = dO / Q MN-major (rows = queries)
+        const uint64_t do_m = sdesc_add(do_mn, so), q_m = sdesc_add(q_mn, so);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tmem + COL_DV, tmem + COL_ST + pcol(kk >> 1) + (kk & 1) * 8,
-                 sdesc_sw128(dos + slot * C::TILE + kk * 16 * 128, HALF, 1024), C::IDESC_TS, (it > 0 || kk > 0));
+          mma_ts(tmem + COL_DV, tmem + COL_ST + pcol(kk >> 1) + (kk & 1) * 8, sdesc_add(do_m, kk * 16 * 128),
+                 C::IDESC_TS, (it > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tmem + COL_DK, tmem + COL_DPT + pcol(kk >> 1) + (kk & 1) * 8,
-                 sdesc_sw128(qs + slot * C::TILE + kk * 16 * 128, HALF, 1024), C::IDESC_TS, (it > 0 || kk > 0));
+          mma_ts(tmem + COL_DK, tmem + COL_DPT + pcol(kk >> 1) + (kk & 1) * 8, sdesc_add(q_m, kk * 16 * 128),
+                 C::IDESC_TS, (it > 0 || kk > 0));
         // dQ = dS K: A = dS (staged as dS^T rows = keys: MN-major), B = K MN-major
         // (rows = keys); 16 keys per instruction
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tmem + COL_ST, sdesc_sw128(dss + kk * 16 * 128, HALF, 1024),
-                 sdesc_sw128(ks + kk * 16 * 128, HALF, 1024), C::IDESC_DQ, kk > 0);
+          mma_ss(tmem + COL_ST, sdesc_add(ds_mn, kk * 16 * 128), sdesc_add(k_mn, kk * 16 * 128), C::IDESC_DQ,
+                 kk > 0);
         tc_commit(dq_full);
       }
       tc_commit(done_bar);
