@@ -78,6 +78,26 @@ def test_running_max_jump_beyond_exp2_range(causal):
     check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what="max jump")
 
 
+@pytest.mark.parametrize("mult", [3.0, 5.0, 8.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_moderate_jumps(mult, causal):
+    """Keys past the first tile scaled by 3, 5 or 8: the row max grows by
+    roughly 8 to 40 log2 units after the first tile, so probabilities far
+    above 1 are exponentiated against a stale running max (and the largest
+    jumps go back over the tile with the new max)."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_prefill(1, 2, 2, 520, 520, 128, seed=int(mult) + 31)
+    k = w["k"].float()
+    k[:, :, 128:] *= mult
+    w["k"] = k.to(torch.bfloat16)
+    q, kk, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, kk, v, causal=causal)
+    assert eta.get_error() == 0
+    Or, Lr = oracle.attention(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                              causal=causal)
+    check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what=f"jump x{mult}")
+
+
 def test_k_outliers():
     run(1, 4, 1, 512, 512, 128, True, seed=12, k_outlier=0.01)
 
