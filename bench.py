@@ -317,7 +317,9 @@ def run_chunked_prefill(steps, warmup, flush, peaks):
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Sk": Sk, "D": D, "causal": True},
         "roofline": {"bound": "tensor", "kernel": "fwd_kernel<Bf16,128>", "achieved": ach,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                     "peak_source": peaks["source"] + " bf16 burst", "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst",
+                     "traffic": dram_traffic("fwd_kernel<Bf16,128>", name,
+                                             source_digest("fwd_kernel.cuh", "fwd_bf16.cu", "ptx.cuh")),
                      "algorithmic_flops": flops, "algorithmic_bytes": acc.prefill_bytes(B, Hq, Hkv, Sq, Sk, D)},
         "gpu_launches": len(ts),
     }
