@@ -634,7 +634,8 @@ def main():
         elif args.only == "fp8_prefill":
             res = run_fp8(args.steps, args.warmup, flush, peaks)
         else:
-            res = run_prefill(args.only, args.steps, args.warmup, flush, peaks)
+            res = run_prefill(args.only, args.steps, args.warmup, flush, peaks,
+                              e2e_steps=args.e2e_steps if args.only == HEADLINE else 0)
         if rank == 0:
             add_spec(res.get("roofline"))
             print(json.dumps(dict(res, only=args.only)), flush=True)
