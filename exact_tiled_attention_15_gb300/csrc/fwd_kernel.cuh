@@ -37,6 +37,7 @@
 // rounding (so they stay in e4m3's normal range and carry the value tile's
 // scale), and the output is multiplied back by max_j sv_j / 2^4.
 #pragma once
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <math_constants.h>
@@ -105,6 +106,7 @@ struct Params {
   float *lse;
   const float *q_scale, *k_scale, *v_scale;  // FP8 only
   int B, Hq, Hkv, Sq, Sk, causal, g, nqb, nqt, nkt;
+  int hc;  // (batch, head) pairs per launch-order chunk
   float scale_log2;
   uint64_t timeout_ns;
   unsigned *err;
@@ -137,10 +139,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *done_bar = o_full + NQT;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
-  const int bh = blockIdx.y;  // b * Hq + hq
+  // Launch order: (batch, head) pairs in chunks of p.hc, whose K and V fit in
+  // L2 together; inside a chunk the latest (heaviest, under a causal mask)
+  // query blocks of all its heads first, so the light ones end the launch.
+  int bh, qx;
+  {
+    const long lin = (long)blockIdx.y * gridDim.x + blockIdx.x, per_chunk = (long)p.hc * p.nqb;
+    const long chunk = lin / per_chunk, r = lin % per_chunk;
+    const long heads = min((long)p.hc, (long)gridDim.y - chunk * p.hc);  // pairs in this chunk
+    qx = (int)(r / heads);
+    bh = (int)(chunk * p.hc + r % heads);  // b * Hq + hq
+  }
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int hkv = hq / p.g;
-  const int q0 = (p.nqb - 1 - (int)blockIdx.x) * (NQT * BM);  // latest (heaviest) query blocks first
+  const int q0 = (p.nqb - 1 - qx) * (NQT * BM);
   const int off = p.Sk - p.Sq;                                 // causal alignment: key j <= row + off
   // key tiles each Q tile visits (a prefix 0 .. nkv_t[i]-1)
   int nkv_t[NQT];
@@ -487,6 +499,16 @@ cudaError_t launch(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   p.nqt = (a.Sq + BM - 1) / BM;
   p.nkt = (a.Sk + BN - 1) / BN;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  // chunks of (batch, head) pairs whose K and V take ~48 MB of L2, used when
+  // the causal mask makes the lightest query block cost under half the
+  // heaviest; otherwise all blocks cost about the same and the order stays
+  // head by head (a head's blocks then share its K and V in L2 at once)
+  {
+    const bool skewed = a.causal && 2L * std::max(0L, (long)a.Sk - a.Sq + NQT * BM) < (long)a.Sk;
+    const double kv_per_head = 2.0 * a.Sk * D * T::kElem / p.g;
+    const long hc = skewed ? (long)(48.0e6 / kv_per_head) : 1;
+    p.hc = (int)std::max(1L, std::min(hc, (long)a.B * a.Hq));
+  }
   p.timeout_ns = a.timeout_ns;
   p.err = a.err;
   if ((long)a.B * a.Hq > 65535) return cudaErrorNotSupported;
