@@ -421,3 +421,78 @@ def test_decode_seqlens_recipe():
     sl = rng.integers(1024, 8193, size=64)
     assert sl.min() >= 1024 and sl.max() <= 8192
     assert int(sl.sum()) == 299418
+
+
+# ---------------------------------------------------------------- rotation convention and row blocks
+def _popcount(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x, dtype=np.int64)
+    c = np.zeros_like(x)
+    while x.any():
+        c += x & 1
+        x = x >> 1
+    return c
+
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16, 32, 64, 128])
+def test_hadamard_is_sylvester_closed_form(n):
+    """Sylvester's construction has the closed form H[i, j] = (-1)^popcount(i & j)
+    (the bits of i and j, one factor [[1, 1], [1, -1]] per bit).  This fixes the
+    order of the blocks: a matrix built as [[H, H], [-H, H]] is also orthogonal
+    and fails here."""
+    i, j = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    expect = np.where(_popcount(i & j) % 2 == 0, 1.0, -1.0)
+    np.testing.assert_array_equal(oracle.quant.hadamard(n), expect)
+
+
+def test_rotation_acts_as_hadamard_then_column_signs():
+    """The rotation is y = x H_D diag(s) / sqrt(D): the unit row e_i goes to
+    s_j (-1)^popcount(i & j) / sqrt(D) in column j.  Signs applied to the rows
+    instead (diag(s) H) would give s_i (...) and fail for any non-constant s.
+    Every one of the 128 unit rows is checked (S = 128 rows of one tile)."""
+    D = 128
+    signs = np.random.default_rng(45).integers(0, 2, D) * 2.0 - 1.0
+    assert 0 < (signs > 0).sum() < D
+    x = np.eye(D)[None, None]                                      # row i = e_i
+    _, _, y = oracle.rotate_quantize(x, signs)
+    i, j = np.meshgrid(np.arange(D), np.arange(D), indexing="ij")
+    expect = signs[None, :] * np.where(_popcount(i & j) % 2 == 0, 1.0, -1.0) / np.sqrt(D)
+    np.testing.assert_allclose(y[0, 0], expect, rtol=0, atol=1e-15)
+    # the code path: every entry has magnitude 1/sqrt(128), so every code is +-448
+    codes, scales, _ = oracle.rotate_quantize(x, signs)
+    np.testing.assert_allclose(scales[0, 0, 0, 0], (1 / np.sqrt(D)) / 448.0, rtol=1e-15)
+    np.testing.assert_array_equal(oracle.e4m3_decode(codes[0, 0]), 448.0 * np.sign(expect))
+
+
+@pytest.mark.parametrize("Sq,Sk", [(37, 53), (53, 37), (37, 37)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_blocks_do_not_change_the_result(Sq, Sk, causal):
+    """attention() forms complete score rows `row_block` at a time only to bound
+    memory.  Any block size gives the same numbers up to the summation order
+    the matrix library picks for a different number of rows (~1e-16), including
+    the causal offset Sk - Sq and rows with no key when Sq > Sk; a
+    block-relative row index in the mask fails here by O(1)."""
+    q, k, v = rand(2, 4, Sq, 16, seed=46), rand(2, 2, Sk, 16, seed=47), rand(2, 2, Sk, 16, seed=48)
+    O1, L1 = oracle.attention(q, k, v, causal=causal, row_block=10 ** 6)
+    for rb in (1, 7, 10, 36):
+        O2, L2 = oracle.attention(q, k, v, causal=causal, row_block=rb)
+        np.testing.assert_allclose(O2, O1, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(L2, L1, rtol=1e-13, atol=1e-14)
+        np.testing.assert_array_equal(np.isneginf(L2), np.isneginf(L1))
+
+
+def test_default_row_block_beyond_one_block_matches_online_pass():
+    """Sq = 1100 > the default block of 1024 rows (the path the long workloads
+    take): the plain definition equals the independent online-softmax pass, and
+    the causal rows past the first block keep their absolute positions."""
+    Sq = Sk = 1100
+    q, k, v = rand(1, 2, Sq, 8, seed=49), rand(1, 1, Sk, 8, seed=50), rand(1, 1, Sk, 8, seed=51)
+    for causal in (False, True):
+        O, L = oracle.attention(q, k, v, causal=causal)
+        O2, L2 = oracle.attention_online(q, k, v, causal=causal, block=128)
+        np.testing.assert_allclose(O, O2, rtol=1e-12, atol=TOL)
+        np.testing.assert_allclose(L, L2, rtol=1e-12, atol=TOL)
+    # row 1030 (second block) under the causal mask sees exactly keys 0..1030
+    O, L = oracle.attention(q, k, v, causal=True)
+    Oi, Li = oracle.attention(q[:, :, 1030:1031], k[:, :, :1031], v[:, :, :1031], causal=False)
+    np.testing.assert_allclose(O[:, :, 1030], Oi[:, :, 0], atol=TOL)
+    np.testing.assert_allclose(L[:, :, 1030], Li[:, :, 0], atol=TOL)
