@@ -96,6 +96,38 @@ def _need(t, name, dtype, dims):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_like(t, name, dtype, shape, device):
+    """A caller-supplied input or output: right dtype, exact shape, contiguous,
+    on the same device as the query -- the library writes through its raw
+    pointer and trusts these."""
+    _need(t, name, dtype, len(shape))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _need_workspace(t, name, nbytes, device):
+    """Caller-supplied scratch: a contiguous CUDA tensor on `device` of at least
+    `nbytes` bytes (the library also checks the byte count it is given)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, {nbytes} needed")
+
+
+def _out(t, name, dtype, shape, device):
+    """The given output tensor after checking it, or a new one."""
+    if t is None:
+        return torch.empty(shape, device=device, dtype=dtype)
+    _need_like(t, name, dtype, shape, device)
+    return t
+
+
 def fwd(q, k, v, causal=False, scale=None, return_lse=True, out=None, lse_out=None):
     """bf16 prefill forward.  q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] -> (o, lse)."""
     _need(q, "q", torch.bfloat16, 4)
@@ -105,11 +137,11 @@ def fwd(q, k, v, causal=False, scale=None, return_lse=True, out=None, lse_out=No
     Hkv, Sk = k.shape[1], k.shape[2]
     if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
         raise ValueError("k and v must be [B, Hkv, Sk, D] matching q")
+    _need_like(k, "k", torch.bfloat16, k.shape, q.device)
+    _need_like(v, "v", torch.bfloat16, k.shape, q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    o = out if out is not None else torch.empty_like(q)
-    lse = None
-    if return_lse:
-        lse = lse_out if lse_out is not None else torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
+    o = _out(out, "out", torch.bfloat16, q.shape, q.device)
+    lse = _out(lse_out, "lse_out", torch.float32, (B, Hq, Sq), q.device) if return_lse else None
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
                         1 if causal else 0, scale, _stream(q.device))
     _check(st, "attn_fwd")
@@ -149,9 +181,15 @@ def fwd_host(q, k, v, causal=False, scale=None, out=None, lse_out=None, workspac
     o = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     lse = lse_out if lse_out is not None else torch.empty(B, Hq, Sq, dtype=torch.float32, pin_memory=True)
     _need_host(o, "out", torch.bfloat16, 4)
+    _need_host(lse, "lse_out", torch.float32, 3)
+    if tuple(o.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("out must be shaped like q and lse_out [B, Hq, Sq]")
     nbytes = fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D)
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _need_workspace(workspace, "workspace", nbytes, dev)
     st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
                              Sq, Sk, D, 1 if causal else 0, scale, _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(dev))
@@ -166,10 +204,18 @@ def bwd(q, k, v, o, lse, dout, causal=False, scale=None, workspace=None):
     _need(lse, "lse", torch.float32, 3)
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Hkv, Sk, D] matching q")
+    for name, t in (("k", k), ("v", v)):
+        _need_like(t, name, torch.bfloat16, k.shape, q.device)
+    for name, t in (("o", o), ("dout", dout)):
+        _need_like(t, name, torch.bfloat16, q.shape, q.device)
+    _need_like(lse, "lse", torch.float32, (B, Hq, Sq), q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     nbytes = int(lib().attn_bwd_workspace_bytes(B, Hq, Sq, D))
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    _need_workspace(workspace, "workspace", nbytes, q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, Sq, Sk, D, 1 if causal else 0, scale, _ptr(workspace),
@@ -194,14 +240,16 @@ def decode(q, kcache, vcache, seqlens, scale=None, workspace=None, return_lse=Tr
         raise ValueError("kcache and vcache must be [B, Hkv, Lmax, D] matching q")
     if seqlens.shape[0] != B:
         raise ValueError("seqlens must have B entries")
+    for name, t in (("kcache", kcache), ("vcache", vcache)):
+        _need_like(t, name, torch.bfloat16, kcache.shape, q.device)
+    _need_like(seqlens, "seqlens", torch.int32, (B,), q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     nbytes = decode_workspace_bytes(B, Hq, Hkv, Lmax, D)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
-    o = out if out is not None else torch.empty_like(q)
-    lse = None
-    if return_lse:
-        lse = lse_out if lse_out is not None else torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    _need_workspace(workspace, "workspace", nbytes, q.device)
+    o = _out(out, "out", torch.bfloat16, q.shape, q.device)
+    lse = _out(lse_out, "lse_out", torch.float32, (B, Hq), q.device) if return_lse else None
     st = lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), _ptr(lse),
                            B, Hq, Hkv, Lmax, D, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(q.device))
@@ -209,7 +257,8 @@ def decode(q, kcache, vcache, seqlens, scale=None, workspace=None, return_lse=Tr
     return o, lse
 
 
-def decode_multi(q, kcache, vcache, seqlens, causal=True, scale=None, workspace=None, return_lse=True):
+def decode_multi(q, kcache, vcache, seqlens, causal=True, scale=None, workspace=None, return_lse=True, out=None,
+                 lse_out=None):
     """T query tokens per sequence: q [B,Hq,T,D] against cache [B,Hkv,Lmax,D] -> (o [B,Hq,T,D], lse [B,Hq,T])."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kcache, "kcache", torch.bfloat16, 4)
@@ -221,12 +270,16 @@ def decode_multi(q, kcache, vcache, seqlens, causal=True, scale=None, workspace=
         raise ValueError("kcache and vcache must be [B, Hkv, Lmax, D] matching q")
     if seqlens.shape[0] != B:
         raise ValueError("seqlens must have B entries")
+    for name, t in (("kcache", kcache), ("vcache", vcache)):
+        _need_like(t, name, torch.bfloat16, kcache.shape, q.device)
+    _need_like(seqlens, "seqlens", torch.int32, (B,), q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     nbytes = int(lib().attn_decode_multi_workspace_bytes(B, Hq, Hkv, T, Lmax, D))
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
-    o = torch.empty_like(q)
-    lse = torch.empty(B, Hq, T, device=q.device, dtype=torch.float32) if return_lse else None
+    _need_workspace(workspace, "workspace", nbytes, q.device)
+    o = _out(out, "out", torch.bfloat16, q.shape, q.device)
+    lse = _out(lse_out, "lse_out", torch.float32, (B, Hq, T), q.device) if return_lse else None
     st = lib().attn_decode_multi(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv,
                                  T, Lmax, D, 1 if causal else 0, scale, _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(q.device))
@@ -250,14 +303,17 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, scale=None, workspac
         raise ValueError("k_pages and v_pages must be [num_pages, Hkv, page_size, D] matching q")
     if block_table.shape[0] != B or seqlens.shape[0] != B:
         raise ValueError("block_table and seqlens must have B rows")
+    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        _need_like(t, name, torch.bfloat16, k_pages.shape, q.device)
+    _need_like(block_table, "block_table", torch.int32, (B, max_blocks), q.device)
+    _need_like(seqlens, "seqlens", torch.int32, (B,), q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     nbytes = decode_workspace_bytes(B, Hq, Hkv, max_blocks * page_size, D)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
-    o = out if out is not None else torch.empty_like(q)
-    lse = None
-    if return_lse:
-        lse = lse_out if lse_out is not None else torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    _need_workspace(workspace, "workspace", nbytes, q.device)
+    o = _out(out, "out", torch.bfloat16, q.shape, q.device)
+    lse = _out(lse_out, "lse_out", torch.float32, (B, Hq), q.device) if return_lse else None
     st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), _ptr(o),
                                  _ptr(lse), B, Hq, Hkv, page_size, max_blocks, num_pages, D, scale, _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(q.device))
@@ -279,18 +335,20 @@ def decode_noalloc(q, kcache, vcache, seqlens, scale=None, return_lse=True, out=
         raise ValueError("kcache and vcache must be [B, Hkv, Lmax, D] matching q")
     if seqlens.shape[0] != B:
         raise ValueError("seqlens must have B entries")
+    for name, t in (("kcache", kcache), ("vcache", vcache)):
+        _need_like(t, name, torch.bfloat16, kcache.shape, q.device)
+    _need_like(seqlens, "seqlens", torch.int32, (B,), q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    o = out if out is not None else torch.empty_like(q)
-    lse = None
-    if return_lse:
-        lse = lse_out if lse_out is not None else torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    o = _out(out, "out", torch.bfloat16, q.shape, q.device)
+    lse = _out(lse_out, "lse_out", torch.float32, (B, Hq), q.device) if return_lse else None
     st = lib().attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), _ptr(lse),
                                    B, Hq, Hkv, Lmax, D, scale, _stream(q.device))
     _check(st, "attn_decode_noalloc")
     return o, lse
 
 
-def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, return_lse=True):
+def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, return_lse=True, out=None,
+            lse_out=None):
     """FP8 e4m3 prefill: codes (uint8) plus one fp32 scale per 128x128 tile -> (o bf16, lse)."""
     for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
         _need(t, name, torch.uint8, 4)
@@ -304,9 +362,13 @@ def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, ret
     if tuple(q_scale.shape) != (B, Hq, nt(Sq), nt(D)) or tuple(k_scale.shape) != (B, Hkv, nt(Sk), nt(D)) \
             or tuple(v_scale.shape) != (B, Hkv, nt(Sk), nt(D)):
         raise ValueError("scales must be [B, H, ceil(S/128), ceil(D/128)]")
+    for name, t in (("k8", k8), ("v8", v8)):
+        _need_like(t, name, torch.uint8, k8.shape, q8.device)
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _need_like(t, name, torch.float32, t.shape, q8.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    o = torch.empty(B, Hq, Sq, D, device=q8.device, dtype=torch.bfloat16)
-    lse = torch.empty(B, Hq, Sq, device=q8.device, dtype=torch.float32) if return_lse else None
+    o = _out(out, "out", torch.bfloat16, (B, Hq, Sq, D), q8.device)
+    lse = _out(lse_out, "lse_out", torch.float32, (B, Hq, Sq), q8.device) if return_lse else None
     st = lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
                             _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, 1 if causal else 0, scale,
                             _stream(q8.device))
@@ -323,9 +385,9 @@ def rotate_quantize_fp8(x, signs=None, codes=None, scales=None):
         _need(signs, "signs", torch.float32, 1)
         if signs.shape[0] != D:
             raise ValueError("signs must have D entries")
-    codes = codes if codes is not None else torch.empty(B, H, S, D, device=x.device, dtype=torch.uint8)
-    scales = scales if scales is not None else torch.empty(B, H, -(-S // 128), 1, device=x.device,
-                                                           dtype=torch.float32)
+        _need_like(signs, "signs", torch.float32, (D,), x.device)
+    codes = _out(codes, "codes", torch.uint8, (B, H, S, D), x.device)
+    scales = _out(scales, "scales", torch.float32, (B, H, -(-S // 128), 1), x.device)
     st = lib().attn_rotate_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), _ptr(signs), B, H, S, D,
                                         _stream(x.device))
     _check(st, "attn_rotate_quantize_fp8")

@@ -3,9 +3,15 @@
 bf16 outputs: |O_gpu - O_ref| <= 1e-2 + half a bf16 ulp of O_ref, elementwise.
 The 1e-2 is the stated bound for bf16 inputs with fp32 accumulation; the
 half-ulp term is the rounding of the output itself to bf16 (8 significant
-bits), which alone exceeds 1e-2 once |O| >= 4.  LSE (fp32): |dLSE| <= 1e-3.
+bits), which alone exceeds 1e-2 once |O| >= 4.  Every check reports the plain
+max |O_gpu - O_ref| beside it, and how many elements lay above 1e-2 and so
+needed the half-ulp term.  LSE (fp32): |dLSE| <= 1e-3.
 FP8 outputs: ||O_gpu - O_ref||_F / ||O_ref||_F <= 5e-2 over the whole tensor.
 """
+from __future__ import annotations
+
+from dataclasses import dataclass
+
 import numpy as np
 
 O_ABS = 1e-2
@@ -19,8 +25,26 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
-    """Assert the bf16 bound; returns (max |dO|, max |dLSE|)."""
+@dataclass
+class Bf16Report:
+    """What one or more bf16 checks saw."""
+    max_abs: float = 0.0    # plain max |O_gpu - O_ref|
+    max_lse: float = 0.0    # max |LSE_gpu - LSE_ref| over finite rows
+    n_half_ulp: int = 0     # elements with |dO| > 1e-2 (inside 1e-2 + half ulp)
+    n: int = 0              # elements compared
+
+    def merge(self, other: "Bf16Report") -> "Bf16Report":
+        return Bf16Report(max(self.max_abs, other.max_abs), max(self.max_lse, other.max_lse),
+                          self.n_half_ulp + other.n_half_ulp, self.n + other.n)
+
+    def __str__(self):
+        return (f"max|dO| {self.max_abs:.4g} (plain), {self.n_half_ulp} of {self.n} elements above 1e-2 "
+                f"within the half-ulp term, max|dLSE| {self.max_lse:.3g}")
+
+
+def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what="") -> Bf16Report:
+    """Assert the bf16 bound; returns what was seen (plain max-abs error, the
+    count of elements that needed the half-ulp term, max LSE error)."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert o_gpu.shape == o_ref.shape, (o_gpu.shape, o_ref.shape)
@@ -30,7 +54,7 @@ def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
     bad = err > bound
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outputs beyond bound; "
                            f"max err {err.max():.3g} at {np.unravel_index(err.argmax(), err.shape)}")
-    dl = 0.0
+    rep = Bf16Report(float(err.max()) if err.size else 0.0, 0.0, int((err > O_ABS).sum()), int(err.size))
     if lse_ref is not None:
         lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
         lse_ref = np.asarray(lse_ref, dtype=np.float64)
@@ -38,9 +62,9 @@ def check_bf16(o_gpu, o_ref, lse_gpu=None, lse_ref=None, what=""):
         assert same_inf.all(), f"{what}: -inf pattern of LSE differs"
         fin = np.isfinite(lse_ref)
         if fin.any():
-            dl = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max())
-        assert dl <= LSE_ABS, f"{what}: LSE max err {dl:.3g}"
-    return float(err.max()), dl
+            rep.max_lse = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max())
+        assert rep.max_lse <= LSE_ABS, f"{what}: LSE max err {rep.max_lse:.3g}"
+    return rep
 
 
 def rel_rms(o_gpu, o_ref) -> float:

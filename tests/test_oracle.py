@@ -496,3 +496,17 @@ def test_default_row_block_beyond_one_block_matches_online_pass():
     Oi, Li = oracle.attention(q[:, :, 1030:1031], k[:, :, :1031], v[:, :, :1031], causal=False)
     np.testing.assert_allclose(O[:, :, 1030], Oi[:, :, 0], atol=TOL)
     np.testing.assert_allclose(L[:, :, 1030], Li[:, :, 0], atol=TOL)
+
+
+def test_process_pool_runs_the_same_definition_per_head():
+    """oracle.pool fans whole heads over spawned worker processes; it must
+    return exactly what the serial definition returns for those heads
+    (GQA, causal with Sq != Sk, a subset of heads in any order)."""
+    from oracle import pool
+    q, k, v = rand(2, 4, 40, 16, seed=52), rand(2, 2, 57, 16, seed=53), rand(2, 2, 57, 16, seed=54)
+    O, L = oracle.attention(q, k, v, causal=True, scale=0.3)
+    heads = [(1, 3), (0, 0), (0, 2), (1, 1)]
+    Op, Lp = pool.attention_heads(q, k, v, heads, causal=True, scale=0.3, workers=2)
+    for i, (b, h) in enumerate(heads):
+        np.testing.assert_array_equal(Op[i], O[b, h])
+        np.testing.assert_array_equal(Lp[i], L[b, h])
