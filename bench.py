@@ -160,6 +160,86 @@ class ClockSampler:
         return out
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (read-only queries)
+    every ~1 ms on a host thread, so that even a leg whose timed steps last a
+    few milliseconds gets samples of its own.  Unavailable without the NVML
+    library; then every query returns None and the nvidia-smi sampler stands."""
+    # clock-event reason bits (nvml.h): the ones a timing must be rejected or noted for
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        import ctypes
+        import threading
+        self.samples = []  # (perf_counter, sm_mhz, reasons bitmask)
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            bus = self._pci_bus_id(device_index)
+            if bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(h)) != 0:
+                    return
+            self._nv, self._h, self._ct = nv, h, ctypes
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._reasons_fn = fn
+            self.sm_max = self._query(nv.nvmlDeviceGetMaxClockInfo)
+            self.ok = self._query(nv.nvmlDeviceGetClockInfo) is not None
+        except Exception:
+            self.ok = False
+
+    @staticmethod
+    def _pci_bus_id(device_index):
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(device_index)
+            return "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            return None
+
+    def _query(self, fn):
+        v = self._ct.c_uint()
+        return v.value if fn(self._h, self._ct.c_int(1), self._ct.byref(v)) == 0 else None  # 1 = SM clock
+
+    def _loop(self):
+        ct = self._ct
+        r = ct.c_ulonglong()
+        while not self._stop.is_set():
+            mhz = self._query(self._nv.nvmlDeviceGetClockInfo)
+            reasons = r.value if self._reasons_fn(self._h, ct.byref(r)) == 0 else 0
+            self.samples.append((time.perf_counter(), mhz, reasons))
+            time.sleep(0.001)
+
+    def start(self):
+        if self.ok:
+            import threading
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
+
+    def window(self, t0, t1):
+        """Median SM MHz, sample count and active reasons inside [t0, t1]."""
+        sel = [(m, r) for t, m, r in self.samples if t0 <= t <= t1 and m is not None]
+        if not sel:
+            return {"sm_mhz": None, "samples": 0, "reasons": []}
+        reasons = sorted({name for _, r in sel for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in sel), "samples": len(sel), "reasons": reasons}
+
+
+# timed windows of the legs (perf_counter seconds), for binning clock samples
+LEG_WINDOWS = {}
+
+
 def source_digest(*names) -> str:
     h = hashlib.sha256()
     for n in names:
@@ -181,20 +261,25 @@ def dram_traffic(kernel: str, workload: str, digest: str):
 
 
 # ---------------------------------------------------------------- timing core
-def time_steps(fn, steps, warmup, flush):
-    """Per-step device time (ms) of fn() on the current stream, L2 flushed between steps."""
+def time_steps(fn, steps, warmup, flush, leg=None):
+    """Per-step device time (ms) of fn() on the current stream, L2 flushed
+    between steps.  With ``leg``, the host-clock window of the timed steps is
+    kept in LEG_WINDOWS[leg] (for the clock samples)."""
     import torch
     st = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0 = time.perf_counter()
     for a, b in evs:
         flush.zero_()
         a.record(st)
         fn()
         b.record(st)
     torch.cuda.synchronize()
+    if leg is not None:
+        LEG_WINDOWS[leg] = (t0, time.perf_counter())
     return [a.elapsed_time(b) for a, b in evs]
 
 
@@ -237,7 +322,7 @@ def timing_stats(ts):
     return {"ms_median": statistics.median(ts), "ms_p95": p95, "ms_ci95": ci}
 
 
-def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
+def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0, leg="same"):
     import torch
     import exact_tiled_attention_15_gb300 as eta
     from exact_tiled_attention_15_gb300 import accounting as acc, workloads
@@ -249,7 +334,7 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
     fn = lambda: eta.fwd(q, k, v, causal=causal, out=o, lse_out=lse)  # noqa: E731
-    ts = time_steps(fn, steps, warmup, flush)
+    ts = time_steps(fn, steps, warmup, flush, leg=name if leg == "same" else leg)
     if eta.get_error() != 0:
         raise RuntimeError(f"{name}: device-side error")
     flops = acc.prefill_flops(B, Hq, S, S, D, causal)
@@ -279,7 +364,7 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0):
         def e2e():
             eta.fwd_host(hq_, hk_, hv_, causal=causal, out=ho, lse_out=hl, workspace=ws, device=dev)
 
-        te = time_steps(e2e, e2e_steps, 2, flush)
+        te = time_steps(e2e, e2e_steps, 2, flush, leg="e2e")
         em = statistics.mean(te)
         res["e2e"] = {"value": flops / (em * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": em,
                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q, k, v)),
@@ -305,7 +390,7 @@ def run_chunked_prefill(steps, warmup, flush, peaks):
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, Sq, device=dev, dtype=torch.float32)
     fn = lambda: eta.fwd(q, k, v, causal=True, out=o, lse_out=lse)  # noqa: E731
-    ts = time_steps(fn, steps, warmup, flush)
+    ts = time_steps(fn, steps, warmup, flush, leg=name)
     if eta.get_error() != 0:
         raise RuntimeError(f"{name}: device-side error")
     flops = acc.prefill_flops_exact(B, Hq, Sq, Sk, D, True)
@@ -342,7 +427,7 @@ def run_backward(steps, warmup, flush, peaks):
     o, lse = eta.fwd(q, k, v, causal=causal)
     ws = torch.empty(int(eta.lib().attn_bwd_workspace_bytes(B, Hq, S, D)), dtype=torch.uint8, device=dev)
     fn = lambda: eta.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws)  # noqa: E731
-    ts = time_steps(fn, steps, warmup, flush)
+    ts = time_steps(fn, steps, warmup, flush, leg=name + "_backward")
     if eta.get_error() != 0:
         raise RuntimeError("backward: device-side error")
     flops = acc.backward_flops(B, Hq, S, S, D, causal)
@@ -377,7 +462,7 @@ def run_decode(steps, warmup, flush, peaks):
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, device=dev, dtype=torch.float32)
     fn = lambda: eta.decode(q, kc, vc, sl, workspace=ws, out=o, lse_out=lse)  # noqa: E731
-    ts = time_steps(fn, steps, warmup, flush)
+    ts = time_steps(fn, steps, warmup, flush, leg=name)
     if eta.get_error() != 0:
         raise RuntimeError("decode: device-side error")
     seqlens = w["seqlens"].tolist()
@@ -416,7 +501,7 @@ def run_decode_paged(steps, warmup, flush, peaks):
     lse = torch.empty(B, Hq, device=dev, dtype=torch.float32)
     fn = lambda: eta.decode_paged(t["q"], t["k_pages"], t["v_pages"], t["block_table"], t["seqlens"],  # noqa: E731
                                   workspace=ws, out=o, lse_out=lse)
-    ts = time_steps(fn, steps, warmup, flush)
+    ts = time_steps(fn, steps, warmup, flush, leg=name)
     if eta.get_error() != 0:
         raise RuntimeError("paged decode: device-side error")
     seqlens = w["seqlens"].tolist()
@@ -450,8 +535,10 @@ def run_decode_multi(steps, warmup, flush, peaks, T=4):
     q, kc, vc, sl = (w[n].to(dev) for n in ("q", "kcache", "vcache", "seqlens"))
     ws = torch.empty(int(eta.lib().attn_decode_multi_workspace_bytes(B, Hq, Hkv, T, cfg["Lmax"], D)),
                      dtype=torch.uint8, device=dev)
-    fn = lambda: eta.decode_multi(q, kc, vc, sl, causal=True, workspace=ws)  # noqa: E731
-    ts = time_steps(fn, steps, warmup, flush)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, T, device=dev, dtype=torch.float32)
+    fn = lambda: eta.decode_multi(q, kc, vc, sl, causal=True, workspace=ws, out=o, lse_out=lse)  # noqa: E731
+    ts = time_steps(fn, steps, warmup, flush, leg=name + f"_T{T}")
     if eta.get_error() != 0:
         raise RuntimeError("multi-token decode: device-side error")
     seqlens = w["seqlens"].tolist()
@@ -491,7 +578,7 @@ def run_quant(steps, warmup, flush, peaks):
         for x, sg, (c, sc) in zip(xs, (signs, signs, None), outs):
             eta.rotate_quantize_fp8(x, sg, codes=c, scales=sc)
 
-    ts = time_steps(fn, steps, warmup, flush)
+    ts = time_steps(fn, steps, warmup, flush, leg="fp8_rotate_quantize")
     if eta.get_error() != 0:
         raise RuntimeError("rotate+quantise: device-side error")
     nbytes = 3 * (B * H * S * D * 3 + B * H * (-(-S // 128)) * 4)  # bf16 read + code write + scales
@@ -521,9 +608,11 @@ def run_fp8(steps, warmup, flush, peaks):
     w = workloads.make_workload(name, seed=0)
     dev = torch.device("cuda")
     t = {n: w[n].to(dev) for n in ("q8", "k8", "v8", "q_scale", "k_scale", "v_scale")}
+    o = torch.empty(B, Hq, S, D, device=dev, dtype=torch.bfloat16)
+    lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
     fn = lambda: eta.fwd_fp8(t["q8"], t["k8"], t["v8"], t["q_scale"], t["k_scale"], t["v_scale"],  # noqa: E731
-                             causal=causal)
-    ts = time_steps(fn, steps, warmup, flush)
+                             causal=causal, out=o, lse_out=lse)
+    ts = time_steps(fn, steps, warmup, flush, leg=name)
     if eta.get_error() != 0:
         raise RuntimeError("fp8: device-side error")
     flops = acc.prefill_flops(B, Hq, S, S, D, causal)
@@ -550,8 +639,9 @@ _INPUT_CACHE = {}
 
 
 def oracle_head_sample(name, budget_s=10.0, max_heads=None):
-    """The fp64 oracle over whole (b, h) heads of the workload until budget_s
-    has elapsed; returns (TFLOP/s, heads, seconds, cores)."""
+    """The fp64 oracle over whole (b, h) heads of the workload, one head after
+    another (BLAS threads on the host cores), until budget_s has elapsed;
+    returns (TFLOP/s, heads, seconds, cores, flops)."""
     import numpy as np
     import oracle
     from exact_tiled_attention_15_gb300 import accounting as acc, workloads
@@ -578,6 +668,45 @@ def oracle_head_sample(name, budget_s=10.0, max_heads=None):
     return flops / t_total / 1e12, heads, t_total, cores, flops
 
 
+def oracle_pool_sample(name, budget_s=10.0):
+    """The fp64 oracle over whole heads of the workload on a process pool of
+    one single-threaded worker per host core (heads are independent problems):
+    after one untimed round (one head per worker, which also starts them),
+    rounds of one head per worker until budget_s has elapsed.  Returns
+    (TFLOP/s, heads, seconds, workers, flops)."""
+    from exact_tiled_attention_15_gb300 import accounting as acc, workloads
+    from oracle.pool import HeadPool
+    cfg = workloads.WORKLOADS[name]
+    if name not in _INPUT_CACHE:
+        _INPUT_CACHE[name] = workloads.make_workload(name, seed=0)
+    w = _INPUT_CACHE[name]
+    S, D, causal = cfg["S"], cfg["D"], cfg["causal"]
+    order = [(b, h) for b in range(cfg["B"]) for h in range(cfg["Hq"])]
+    with HeadPool(w["q"].float().numpy(), w["k"].float().numpy(), w["v"].float().numpy()) as pool:
+        n = pool.workers
+        pool.run(order[:n], causal, 1.0 / math.sqrt(D))
+        done, t, r = 0, 0.0, 1
+        while t < budget_s:
+            batch = [order[(r * n + i) % len(order)] for i in range(n)]
+            t0 = time.perf_counter()
+            pool.run(batch, causal, 1.0 / math.sqrt(D))
+            t += time.perf_counter() - t0
+            done += n
+            r += 1
+    flops = acc.prefill_flops(1, done, S, S, D, causal)
+    return flops / t / 1e12, done, t, n, flops
+
+
+def headline_config(ws):
+    """The `config` object of the headline line (both arms)."""
+    from exact_tiled_attention_15_gb300 import workloads
+    cfg = workloads.WORKLOADS[HEADLINE]
+    return {"workload": HEADLINE, "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"], "Sq": cfg["S"], "Sk": cfg["S"],
+            "D": cfg["D"], "causal": cfg["causal"],
+            "l2": "flushed between steps (256 MB write outside the timed events); inputs 402 MB also exceed the "
+                  "129 MB L2", "parallelism": f"replicas x{ws}"}
+
+
 def reference_arm(args, ws, rank):
     """--impl reference: the CPU fp64 oracle as it stands, one head of the
     headline workload per step, on this machine's host cores."""
@@ -599,8 +728,7 @@ def reference_arm(args, ws, rank):
         "impl": "reference", "metric": HEADLINE_METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": HEADLINE, "B": 4, "Hq": 32, "Hkv": 32, "Sq": 4096, "Sk": 4096, "D": 128,
-                   "causal": True},
+        "config": headline_config(ws),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": wall,
@@ -642,6 +770,8 @@ def main():
         return
     clocks = ClockSampler(local)
     clocks.start()
+    nvml = NvmlClockSampler(local)
+    nvml.start()
     time.sleep(0.3)
     barrier(ws)
     torch.cuda.synchronize()
@@ -664,7 +794,10 @@ def main():
             extras["fp8_prefill"] = run_fp8(args.steps, args.warmup, flush, peaks)
         except Exception as e:  # reported, not hidden
             extras["fp8_prefill"] = {"error": str(e).splitlines()[0]}
-    e2e = run_prefill(HEADLINE, 1, 1, flush, peaks, e2e_steps=args.e2e_steps)["e2e"] if args.e2e_steps > 0 else None
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_prefill(HEADLINE, 1, 1, flush, peaks, e2e_steps=args.e2e_steps, leg=None)["e2e"]
+    nvml.stop()
     clk = clocks.stop()
     if rank != 0:
         return
@@ -672,32 +805,50 @@ def main():
     for leg in extras.values():
         if isinstance(leg, dict) and "roofline" in leg:
             add_spec(leg["roofline"])
+    # clock samples binned by each leg's timed steps (NVML, ~1 ms apart)
+    leg_clk = {name: nvml.window(*win) for name, win in LEG_WINDOWS.items()} if nvml.ok else {}
+    head_clk = leg_clk.get(HEADLINE, {})
     value = whole_job_tflops(head["flops_per_step"], ws, step_ms)
+    reasons = sorted(set(clk["reasons"]) | {r for c in leg_clk.values() for r in c["reasons"]})
     line = {
         "metric": HEADLINE_METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_ms, "ms_median": head["ms_median"], "ms_p95": head["ms_p95"],
         "ms_ci95": head["ms_ci95"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": dict(head["config"], l2="flushed between steps (256 MB write outside the timed events); "
-                                          "inputs 402 MB also exceed the 129 MB L2",
-                       parallelism=f"replicas x{ws}"),
+        "config": headline_config(ws),
         "roofline": head["roofline"],
         "e2e": None if e2e is None else {
             "value": e2e["value"] * ws, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
             "d2h_bytes_per_step": e2e["d2h_bytes_per_step"], "ms_per_step": e2e["ms_per_step"],
             "api": e2e["api"]},
         "gpu_launches": head["gpu_launches"],
-        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
-                   "samples": clk["samples"]},
+        "clocks": {"sm_mhz": head_clk.get("sm_mhz") or clk["sm_mhz"],
+                   "sm_max_mhz": getattr(nvml, "sm_max", None) or clk["sm_max_mhz"], "reasons": reasons,
+                   "samples": head_clk.get("samples", clk["samples"]),
+                   "how": ("NVML every ~1 ms inside the headline's timed steps" if head_clk.get("samples")
+                           else "nvidia-smi every 200 ms over the run"),
+                   "smi_sm_mhz_median": clk["sm_mhz"], "smi_samples": clk["samples"]},
         "workloads": extras,
         "timed_region_s": region_s,
     }
     if not args.no_cpu_baseline and ws == 1:
-        v, heads, t, cores, _ = oracle_head_sample(HEADLINE, budget_s=10.0)
+        v, heads, t, cores, _ = oracle_pool_sample(HEADLINE, budget_s=10.0)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{heads} full causal head(s) of the headline workload, {t:.1f} s "
-                                          f"of fp64 NumPy (BLAS threads on {cores} cores)"}
+                                "sample": f"{heads} full causal heads of the headline workload in {t:.1f} s: "
+                                          f"the fp64 NumPy oracle on {cores} single-threaded worker processes, "
+                                          f"one head each at a time"}
+    # last: one compact entry per leg, so every figure survives a cut of the line's head
+    legs = {HEADLINE: head, **extras}
+    line["legs"] = {}
+    for name, r in legs.items():
+        if not isinstance(r, dict) or "value" not in r:
+            line["legs"][name] = r
+            continue
+        c = leg_clk.get(name, {})
+        line["legs"][name] = {"value": round(r["value"], 1), "unit": r["unit"],
+                              "frac": round(r["roofline"]["frac"], 4), "ms": round(r["ms_per_step"], 4),
+                              "mhz": c.get("sm_mhz")}
     print(json.dumps(line), flush=True)
 
 

@@ -37,6 +37,7 @@ SIGNATURES = {
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_rotate_quantize_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attn_get_error": (_I, [_P]),
+    "attn_debug_stall_role_waits": (None, [_I]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
     "attn_version": (ctypes.c_char_p, []),
 }
@@ -397,6 +398,12 @@ def rotate_quantize_fp8(x, signs=None, codes=None, scales=None):
 def get_error(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device error word."""
     return int(lib().attn_get_error(_stream(device)))
+
+
+def debug_stall_role_waits(enable: bool) -> None:
+    """Test hook: later forward/backward calls wait for a signal nothing gives
+    (bounded at 1 ms) and report ATTN_ERR_TIMEOUT; False restores them."""
+    lib().attn_debug_stall_role_waits(1 if enable else 0)
 
 
 def version() -> str:

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -19,6 +20,17 @@ namespace {
 __device__ unsigned g_attn_error;
 
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s per pipeline wait
+
+// attn_debug_stall_role_waits: when set, kernels that support it first wait
+// for a signal nothing gives, with the waits between warp roles bounded by
+// kStallWaitNs, so that those waits run out.
+std::atomic<int> g_debug_stall{0};
+constexpr uint64_t kStallWaitNs = 1000000ull;  // 1 ms
+
+uint64_t role_wait_ns() {
+  return g_debug_stall.load(std::memory_order_relaxed) ? kStallWaitNs : kDefaultTimeoutNs;
+}
+int debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -142,6 +154,8 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
   a.causal = causal ? 1 : 0;
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_fwd_bf16(a, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
@@ -335,6 +349,8 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
   a.causal = causal ? 1 : 0;
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_fwd_fp8(a, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
@@ -412,6 +428,8 @@ attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scale
   return from_cuda(attn::launch_rotate_quantize(tmx, tmc, scales, signs, B, H, S, kDefaultTimeoutNs, err,
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
+
+void attn_debug_stall_role_waits(int enable) { g_debug_stall.store(enable ? 1 : 0, std::memory_order_relaxed); }
 
 attn_status attn_get_error(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -39,6 +39,7 @@
 #pragma once
 #include <algorithm>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <math_constants.h>
 
@@ -85,7 +86,7 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NQT * TILE;
   static constexpr int OFF_V = OFF_K + NSK * TILE;
   static constexpr int OFF_BAR = OFF_V + NSV * TILE;
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQT + 1;
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQT + 2;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
   static constexpr int P_REGS = BN * T::kElem / 4;  // 32-bit TMEM columns holding one P row
@@ -108,7 +109,9 @@ struct Params {
   int B, Hq, Hkv, Sq, Sk, causal, g, nqb, nqt, nkt;
   int hc;  // (batch, head) pairs per launch-order chunk
   float scale_log2;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies and on the CTA's own tensor-core work
+  uint64_t wait_ns;     // waits of one role on another (softmax <-> MMA issuer)
+  int stall;            // test hook: the softmax first waits for a signal nothing gives
   unsigned *err;
 };
 
@@ -137,6 +140,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *v_full = k_empty + NSK, *v_empty = v_full + NSV;
   uint64_t *s_full = v_empty + NSV, *p_full = s_full + NQT, *o_full = p_full + NQT;
   uint64_t *done_bar = o_full + NQT;
+  uint64_t *never = done_bar + 1;  // test hook: no thread ever arrives on it
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
   // Launch order: (batch, head) pairs in chunks of p.hc, whose K and V fit in
@@ -194,12 +198,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int i = 0; i < NQT; ++i) {
+    for (int i = 0; i < NQT; ++i) {  // p_full: one arrival per softmax warp
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], BM);
+      mbar_init(&p_full[i], BM / 32);
       mbar_init(&o_full[i], 1);
     }
     mbar_init(done_bar, 1);
+    mbar_init(never, 1);
     mbar_init_fence();
   }
   tc_fence_before();
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // O_i += P_i V_j: P from TMEM (8 columns per instruction), V MN-major
       // (rows = keys; 128-byte slabs of the head dimension HALF bytes apart)
       auto issue_pv = [&](int i, int j) -> bool {
-        if (!mbar_wait(&p_full[i], j & 1, p.timeout_ns, p.err)) return false;
+        if (!mbar_wait(&p_full[i], j & 1, p.wait_ns, p.err)) return false;
         tc_fence_after();
         const int slot = j % NSV;
         const uint64_t dv = sdesc_add(dv0, slot * C::TILE);
@@ -310,6 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_commit(&k_empty[(j + 1) % NSK]);
         }
       }
+      // every product issued above has completed before the CTA moves on
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, p.timeout_ns, p.err);
     }
@@ -334,15 +340,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       sv_ref = fmaxf(mv, 1e-30f);
     }
     float m_use = -CUDART_INF_F;  // running max in log2 units (moved lazily)
-    float l = 0.f;                // running sum relative to m_use
-    bool ok = true;
-    for (int j = 0; j < my_nkv; ++j) {
+    float l = 0.f;                // running sum relative to m_use (gives the LSE)
+    float l_o = 0.f;              // the sum O is divided by (below)
+    // test hook: wait for a signal nothing gives, so that this wait runs out
+    bool ok = !p.stall || __all_sync(0xffffffffu, mbar_wait(never, 0, p.wait_ns, p.err));
+    for (int j = 0; ok && j < my_nkv; ++j) {
       float cj = p.scale_log2, e_off = T::kPre;
       if constexpr (T::kFp8) {
         cj *= cq * __ldg(&p.k_scale[(size_t)zk * p.nkt + j]);
         e_off += __log2f(fmaxf(__ldg(&p.v_scale[(size_t)zk * p.nkt + j]), 1e-30f) / sv_ref);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i], j & 1, p.timeout_ns, p.err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i], j & 1, p.wait_ns, p.err))) {
         ok = false;
         break;
       }
@@ -411,7 +419,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       f2_unpack(acc2[0], r0, r1);
       f2_unpack(acc2[1], r2, r3);
       const float rs = (r0 + r1) + (r2 + r3);
-      l = l * alpha + (T::kFp8 ? rs * fast_exp2(-e_off) : rs);
+      // The tile's largest probability enters P rounded to bf16 (e4m3).  With
+      // the running max moved lazily it is 2^x with 0 < x <= the threshold,
+      // not 1, so its rounding is up to half an ulp of it; the sum that O is
+      // divided by takes that rounding too, so a row dominated by one key
+      // still comes out as that key's value row.  (The LSE keeps the exact sum.)
+      const float pm = fast_exp2(fmaf(mx, cj, bias));  // as computed for that score above
+      float pm_r;
+      if constexpr (T::kFp8) {
+        const __half_raw hr = __nv_cvt_fp8_to_halfraw(__nv_cvt_float_to_fp8(pm, __NV_SATFINITE, __NV_E4M3), __NV_E4M3);
+        pm_r = __half2float(__half(hr));
+      } else {
+        pm_r = __bfloat162float(__float2bfloat16_rn(pm));
+      }
+      const float back = T::kFp8 ? fast_exp2(-e_off) : 1.f;
+      l = l * alpha + rs * back;
+      l_o = l_o * alpha + (rs + (pm_r - pm)) * back;
 #pragma unroll
       for (int c = 0; c < C::P_REGS / 32; ++c) {
         uint32_t chunk[32];
@@ -421,7 +444,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Rescale O_i by alpha once P_{j-1} V_{j-1} has landed (warp-uniform).
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.timeout_ns, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.wait_ns, p.err))) {
+          tmem_st_wait();  // no store of P may still be in flight when the CTA ends
           ok = false;
           break;
         }
@@ -437,14 +461,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i]);
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[i], (my_nkv - 1) & 1, p.timeout_ns, p.err));
+    if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[i], (my_nkv - 1) & 1, p.wait_ns, p.err));
     if (ok) {
       tc_fence_after();
       const float out_scale = T::kFp8 ? sv_ref * fast_exp2(-T::kPre) : 1.f;
-      const float inv = l > 0.f ? out_scale / l : 0.f;
+      const float inv = l_o > 0.f ? out_scale / l_o : 0.f;
       uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + min(row, p.Sq - 1)) * D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -510,6 +535,8 @@ cudaError_t launch(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
     p.hc = (int)std::max(1L, std::min(hc, (long)a.B * a.Hq));
   }
   p.timeout_ns = a.timeout_ns;
+  p.wait_ns = a.wait_ns;
+  p.stall = a.stall;
   p.err = a.err;
   if ((long)a.B * a.Hq > 65535) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

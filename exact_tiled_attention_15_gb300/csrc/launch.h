@@ -48,7 +48,9 @@ struct FwdArgs {
   const float *q_scale, *k_scale, *v_scale;  // FP8 only
   int B, Hq, Hkv, Sq, Sk, D, causal;
   float scale;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies and on a CTA's own tensor-core work
+  uint64_t wait_ns;     // waits of one warp role on another inside a CTA
+  int stall;            // test hook: the softmax first waits for a signal nothing gives
   unsigned *err;
 };
 

@@ -270,6 +270,24 @@ attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scale
  */
 attn_status attn_get_error(attn_stream_t stream);
 
+/*
+ * attn_debug_stall_role_waits -- test hook for the failure path of the
+ * pipelines (no page defines it).  Inside a CTA of the prefill forward
+ * (attn_fwd, attn_fwd_fp8) and the backward (attn_bwd), warp roles wait on
+ * one another (the softmax for the scores, the tensor-core issuer for the
+ * probabilities, ...), each wait bounded in time.  With enable != 0, every
+ * such call made afterwards first has its softmax (backward: gradient) warps
+ * wait for a signal that nothing gives, and the bound of the waits between
+ * roles is cut to 1 ms: those waits run out, the kernel records
+ * ATTN_ERR_TIMEOUT (returned by the next attn_get_error()) and the outputs of
+ * that call are invalid.  Waits for data copies and for a CTA's own
+ * tensor-core work keep the normal bound (4 s), so a CTA that gives up still
+ * lets every copy and product it started complete and frees its tensor
+ * memory before it ends; the GPU context stays usable.  enable = 0 restores
+ * normal operation.  Process-wide; for tests only.
+ */
+void attn_debug_stall_role_waits(int enable);
+
 /* Human-readable name of a status code (static string). */
 const char *attn_status_str(attn_status status);
 

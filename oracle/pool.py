@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import multiprocessing as mp
 import os
+import shutil
 import tempfile
 
 import numpy as np
@@ -24,22 +25,22 @@ _BLAS_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLI
 _W = {}
 
 
-def _init(paths, out_paths):
+def _init(paths):
     _W["q"], _W["k"], _W["v"] = (np.load(p, mmap_mode="r") for p in paths)
-    _W["o"] = np.load(out_paths[0], mmap_mode="r+")
-    _W["l"] = np.load(out_paths[1], mmap_mode="r+")
 
 
 def _one(task):
     from .attention import attention
-    idx, b, h, causal, scale = task
+    idx, b, h, causal, scale, out_paths = task
     q, k, v = _W["q"], _W["k"], _W["v"]
     kv = h // (q.shape[1] // k.shape[1])
     O, L = attention(q[b:b + 1, h:h + 1], k[b:b + 1, kv:kv + 1], v[b:b + 1, kv:kv + 1], causal=causal, scale=scale)
-    _W["o"][idx] = O[0, 0]
-    _W["l"][idx] = L[0, 0]
-    _W["o"].flush()
-    _W["l"].flush()
+    o = np.load(out_paths[0], mmap_mode="r+")
+    lse = np.load(out_paths[1], mmap_mode="r+")
+    o[idx] = O[0, 0]
+    lse[idx] = L[0, 0]
+    o.flush()
+    lse.flush()
     return idx
 
 
@@ -47,39 +48,62 @@ def default_workers() -> int:
     return max(1, len(os.sched_getaffinity(0)))
 
 
-def attention_heads(q, k, v, heads, causal: bool, scale: float | None = None, workers: int | None = None):
-    """O [len(heads), Sq, D] and LSE [len(heads), Sq] (float64) of the listed
-    (b, h) pairs of q [B,Hq,Sq,D] against k/v [B,Hkv,Sk,D] (numpy arrays of any
-    float type; they are read as float64 by the definition)."""
-    heads = [(int(b), int(h)) for b, h in heads]
-    Sq, D = q.shape[2], v.shape[3]
-    if scale is None:
-        scale = 1.0 / np.sqrt(q.shape[3])
-    workers = min(workers or default_workers(), max(1, len(heads)))
-    with tempfile.TemporaryDirectory(prefix="oracle_pool_") as d:
+class HeadPool:
+    """Worker processes holding q [B,Hq,Sq,D] and k/v [B,Hkv,Sk,D] (numpy
+    arrays of any float type, read as float64 by the definition); ``run`` gives
+    O [n, Sq, D] and LSE [n, Sq] (float64) of the listed (b, h) pairs."""
+
+    def __init__(self, q, k, v, workers: int | None = None):
+        self.workers = workers or default_workers()
+        self.shape_q, self.dv = q.shape, v.shape[3]
+        self.dir = tempfile.mkdtemp(prefix="oracle_pool_")
         paths = []
         for name, x in (("q", q), ("k", k), ("v", v)):
-            p = os.path.join(d, name + ".npy")
+            p = os.path.join(self.dir, name + ".npy")
             np.save(p, np.ascontiguousarray(x))
             paths.append(p)
-        out_paths = (os.path.join(d, "o.npy"), os.path.join(d, "l.npy"))
-        np.lib.format.open_memmap(out_paths[0], mode="w+", dtype=np.float64, shape=(len(heads), Sq, D)).flush()
-        np.lib.format.open_memmap(out_paths[1], mode="w+", dtype=np.float64, shape=(len(heads), Sq)).flush()
         saved = {n: os.environ.get(n) for n in _BLAS_VARS}
         try:
             for n in _BLAS_VARS:  # the spawned workers read these when their BLAS loads
                 os.environ[n] = "1"
-            ctx = mp.get_context("spawn")
-            with ctx.Pool(workers, initializer=_init, initargs=(paths, out_paths)) as pool:
-                done = pool.map(_one, [(i, b, h, bool(causal), float(scale)) for i, (b, h) in enumerate(heads)],
-                                chunksize=1)
+            self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_init, initargs=(paths,))
         finally:
             for n, val in saved.items():
                 if val is None:
                     os.environ.pop(n, None)
                 else:
                     os.environ[n] = val
+
+    def run(self, heads, causal: bool, scale: float | None = None):
+        heads = [(int(b), int(h)) for b, h in heads]
+        Sq = self.shape_q[2]
+        if scale is None:
+            scale = 1.0 / np.sqrt(self.shape_q[3])
+        out_paths = (os.path.join(self.dir, "o.npy"), os.path.join(self.dir, "l.npy"))
+        np.lib.format.open_memmap(out_paths[0], mode="w+", dtype=np.float64, shape=(len(heads), Sq, self.dv)).flush()
+        np.lib.format.open_memmap(out_paths[1], mode="w+", dtype=np.float64, shape=(len(heads), Sq)).flush()
+        tasks = [(i, b, h, bool(causal), float(scale), out_paths) for i, (b, h) in enumerate(heads)]
+        done = self.pool.map(_one, tasks, chunksize=1)
         assert sorted(done) == list(range(len(heads)))
         O = np.array(np.load(out_paths[0], mmap_mode="r"))
         L = np.array(np.load(out_paths[1], mmap_mode="r"))
-    return O, L
+        return O, L
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def attention_heads(q, k, v, heads, causal: bool, scale: float | None = None, workers: int | None = None):
+    """O [len(heads), Sq, D] and LSE [len(heads), Sq] (float64) of the listed
+    (b, h) pairs, computed on a pool of at most ``workers`` processes."""
+    workers = min(workers or default_workers(), max(1, len(heads)))
+    with HeadPool(q, k, v, workers) as pool:
+        return pool.run(heads, causal, scale)

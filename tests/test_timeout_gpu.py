@@ -1,0 +1,72 @@
+"""The bounded waits inside the prefill pipelines, made to run out on purpose.
+
+Inside a forward CTA the softmax warps wait for the scores and the tensor-core
+issuer waits for the probabilities.  With attn_debug_stall_role_waits the
+softmax warps first wait for a signal that nothing gives, and the bound of the
+waits between warp roles is 1 ms, so those waits run out (the issuer's wait
+for probabilities too): the kernel must record ATTN_ERR_TIMEOUT, let the
+copies and products it started complete (those waits keep their normal
+bound), free its tensor memory and end.  attn_get_error() then reports the
+timeout once, and an ordinary call in the same process afterwards must be
+correct -- the GPU context survived.
+
+No GPU is faulted, trapped or hung: every wait ends, the stalled ones after
+1 ms.  The sizes keep the K and V rings from ever waiting for a freed slot (at
+most two K and three V tiles per CTA), so no wait with the normal 4 s bound is
+left waiting on a side that gave up.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_15_gb300 import workloads
+from parity import FP8_REL_RMS, check_bf16, rel_rms
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+ATTN_ERR_TIMEOUT = 4
+
+
+def _stalled(fn):
+    import exact_tiled_attention_15_gb300 as eta
+    assert eta.get_error() == 0
+    eta.debug_stall_role_waits(True)
+    try:
+        fn()
+        status = eta.get_error()
+    finally:
+        eta.debug_stall_role_waits(False)
+    return status
+
+
+@pytest.mark.parametrize("S", [128, 256])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_wait_runs_out_then_next_call_is_correct(S, D, causal):
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_prefill(1, 2, 2, S, S, D, seed=S + D)
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    st = _stalled(lambda: eta.fwd(q, k, v, causal=causal))
+    assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
+    assert eta.get_error() == 0  # reported once, then cleared
+    o, lse = eta.fwd(q, k, v, causal=causal)
+    assert eta.get_error() == 0
+    Or, Lr = oracle.attention(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                              causal=causal)
+    check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what=f"after timeout S{S} D{D}")
+
+
+def test_fp8_forward_wait_runs_out_then_next_call_is_correct():
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_fp8_prefill(1, 2, 2, 256, 256, 128, seed=3)
+    t = [w[n].to(DEV) for n in ("q8", "k8", "v8", "q_scale", "k_scale", "v_scale")]
+    st = _stalled(lambda: eta.fwd_fp8(*t))
+    assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
+    assert eta.get_error() == 0
+    o, lse = eta.fwd_fp8(*t)
+    assert eta.get_error() == 0
+    deq = [oracle.dequantize_tiles(w[n + "8"].numpy(), w[n + "_scale"].numpy()) for n in ("q", "k", "v")]
+    Or, Lr = oracle.attention(*deq)
+    assert rel_rms(o.double().cpu().numpy(), Or) <= FP8_REL_RMS
+    assert np.abs(lse.cpu().numpy() - Lr).max() <= 1e-3
