@@ -132,6 +132,7 @@ const char *attn_version(void) { return "0.1.0"; }
 
 attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                      int Sq, int Sk, int D, int causal, float scale, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_fwd");
   attn_status st = check_prefill(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale);
   if (st != ATTN_OK) return st;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
@@ -178,6 +179,7 @@ size_t attn_decode_multi_workspace_bytes(int B, int Hq, int Hkv, int T, int Lmax
 attn_status attn_decode(const void *q, const void *kcache, const void *vcache, const int32_t *seqlens, void *o,
                         float *lse, int B, int Hq, int Hkv, int Lmax, int D, float scale, void *workspace,
                         size_t workspace_bytes, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_decode");
   if (!q || !kcache || !vcache || !seqlens || !o || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || D < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (bad_scale(scale)) return ATTN_ERR_INVALID_ARG;
@@ -222,6 +224,7 @@ attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_
                               const int32_t *seqlens, void *o, float *lse, int B, int Hq, int Hkv, int page_size,
                               int max_blocks, int num_pages, int D, float scale, void *workspace,
                               size_t workspace_bytes, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_decode_paged");
   if (!q || !k_pages || !v_pages || !block_table || !seqlens || !o || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_pages < 1 || D < 1 || Hq % Hkv != 0)
     return ATTN_ERR_INVALID_ARG;
@@ -276,6 +279,7 @@ attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_
 attn_status attn_decode_multi(const void *q, const void *kcache, const void *vcache, const int32_t *seqlens, void *o,
                               float *lse, int B, int Hq, int Hkv, int T, int Lmax, int D, int causal, float scale,
                               void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_decode_multi");
   if (!q || !kcache || !vcache || !seqlens || !o || !workspace) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || D < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (T < 1 || T > 16) return ATTN_ERR_UNSUPPORTED;
@@ -320,6 +324,7 @@ attn_status attn_decode_multi(const void *q, const void *kcache, const void *vca
 attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8, const float *q_scale,
                          const float *k_scale, const float *v_scale, void *o, float *lse, int B, int Hq, int Hkv,
                          int Sq, int Sk, int D, int causal, float scale, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_fwd_fp8");
   attn_status st = check_prefill(q8, k8, v8, o, B, Hq, Hkv, Sq, Sk, D, scale);
   if (st != ATTN_OK) return st;
   if (!q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
@@ -365,6 +370,7 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D) {
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
                      void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                      float scale, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_bwd");
   attn_status st = check_prefill(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale);
   if (st != ATTN_OK) return st;
   if (!lse || !dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
@@ -411,13 +417,14 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
 
 attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
                                      int S, int D, attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_rotate_quantize_fp8");
   if (!x || !codes || !scales) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
       (signs && (reinterpret_cast<uintptr_t>(signs) & 3u)))
     return ATTN_ERR_INVALID_ARG;
   if (D != 128) return ATTN_ERR_UNSUPPORTED;
-  if ((int64_t)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((int64_t)B * H > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;  // TMA plane coordinate
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
   CUtensorMap tmx, tmc;
   if (!make_tmap(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, (uint64_t)B * H, 64, 128) ||

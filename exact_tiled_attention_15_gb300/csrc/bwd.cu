@@ -147,8 +147,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *done_bar = dq_free + 1;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
-  const int j = blockIdx.x;  // key tile
-  const int bkv = blockIdx.y;
+  const int nkt = (p.Sk + BN - 1) / BN;
+  const int j = (int)(blockIdx.x % nkt);    // key tile
+  const int bkv = (int)(blockIdx.x / nkt);  // batch x KV head
   const int b = bkv / p.Hkv, kvh = bkv % p.Hkv;
   const int kj0 = j * BN;
   const int off = p.Sk - p.Sq;  // causal: key k visible to query q iff k <= q + off
@@ -499,10 +500,10 @@ cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
   p.err = a.err;
-  if ((long)a.B * a.Hkv > 65535) return cudaErrorNotSupported;
+  if ((long)((a.Sk + BN - 1) / BN) * a.B * a.Hkv > 0x7fffffffL) return cudaErrorNotSupported;
   e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((a.Sk + BN - 1) / BN), (unsigned)(a.B * a.Hkv));
+  dim3 grid((unsigned)(((a.Sk + BN - 1) / BN) * a.B * a.Hkv));
   bwd_kernel<D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -88,9 +88,12 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint64_t *cbar = empty + NST;  // consumer-warp barrier (bounded, unlike bar.sync)
   int *s_fail = reinterpret_cast<int *>(cbar + 1);
 
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / p.nhc, hc = blockIdx.y % p.nhc;
-  const int b = blockIdx.z;
+  // one-dimensional grid: split fastest, then (KV head, head chunk), then sequence
+  const long cta = blockIdx.x;
+  const int split = (int)(cta % p.nsplit);
+  const long rest = cta / p.nsplit;
+  const int kvh = (int)(rest % ((long)p.Hkv * p.nhc)) / p.nhc, hc = (int)(rest % ((long)p.Hkv * p.nhc)) % p.nhc;
+  const int b = (int)(rest / ((long)p.Hkv * p.nhc));
   // The merge kernel may be scheduled as soon as every CTA of this grid has
   // started; it waits for this grid's results before reading them.
   griddep_launch_dependents();
@@ -441,8 +444,9 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if (a.B > 65535 || (long)a.Hkv * nhc > 65535) return cudaErrorNotSupported;
-  dim3 grid(a.nsplit, a.Hkv * nhc, a.B);
+  const long nctas = (long)a.nsplit * a.Hkv * nhc * a.B;
+  if (nctas > 0x7fffffffL || (long)a.B * a.Hq * a.T > 0x7fffffffL) return cudaErrorNotSupported;
+  dim3 grid((unsigned)nctas);
   decode_split_kernel<D, PAGED><<<grid, THREADS, C::SMEM_BYTES, st>>>(tmk, tmv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -148,9 +148,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   // query blocks of all its heads first, so the light ones end the launch.
   int bh, qx;
   {
-    const long lin = (long)blockIdx.y * gridDim.x + blockIdx.x, per_chunk = (long)p.hc * p.nqb;
+    const long lin = blockIdx.x, per_chunk = (long)p.hc * p.nqb;
     const long chunk = lin / per_chunk, r = lin % per_chunk;
-    const long heads = min((long)p.hc, (long)gridDim.y - chunk * p.hc);  // pairs in this chunk
+    const long heads = min((long)p.hc, (long)p.B * p.Hq - chunk * p.hc);  // pairs in this chunk
     qx = (int)(r / heads);
     bh = (int)(chunk * p.hc + r % heads);  // b * Hq + hq
   }
@@ -538,10 +538,10 @@ cudaError_t launch(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   p.wait_ns = a.wait_ns;
   p.stall = a.stall;
   p.err = a.err;
-  if ((long)a.B * a.Hq > 65535) return cudaErrorNotSupported;
+  if ((long)p.nqb * a.B * a.Hq > 0x7fffffffL) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.nqb, (unsigned)(a.B * a.Hq));
+  dim3 grid((unsigned)((long)p.nqb * a.B * a.Hq));
   fwd_kernel<T, D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

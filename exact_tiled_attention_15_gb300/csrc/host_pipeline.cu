@@ -13,6 +13,7 @@
 #include <cstdint>
 
 #include "../../include/attn.h"
+#include "launch.h"
 
 namespace {
 
@@ -91,6 +92,7 @@ size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int
 attn_status attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                           int Sq, int Sk, int D, int causal, float scale, void *workspace, size_t workspace_bytes,
                           attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_fwd_host");
   Plan p;
   if (!q || !k || !v || !o || !workspace) return ATTN_ERR_INVALID_ARG;
   if (!make_plan(B, Hq, Hkv, Sq, Sk, D, p)) return ATTN_ERR_INVALID_ARG;

@@ -3,10 +3,23 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstddef>
 #include <cstdint>
 
 namespace attn {
+
+// An NVTX range named after the entry point, open for the duration of the
+// call (its host-side work and launches), so that profilers and tracing tools
+// show each call of the library on the timeline.  Costs a pointer check when
+// no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Query heads one decode CTA covers: nhpc * T query rows fit the 16 MMA rows.
 inline int decode_heads_per_cta(int Hq, int Hkv, int T) {

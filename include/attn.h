@@ -28,6 +28,10 @@
  *     failure returns ATTN_ERR_CUDA.  Device-side faults of the pipeline (a
  *     bounded wait that ran out) are recorded in a device error word that
  *     attn_get_error() reads.
+ *   - Size limits: B * Hq and B * Hkv (decode: B * Hq * T; paged: num_pages *
+ *     Hkv) at most 2^30 (the TMA coordinate range) and at most 2^31 - 1 CTAs
+ *     per launch; beyond them a call returns ATTN_ERR_UNSUPPORTED.  There is
+ *     no other limit on the batch or head counts.
  *   - The library is stateless apart from that error word, a per-device
  *     cache of kernel attributes and, for attn_fwd_host, two CUDA streams and
  *     ten events per calling thread and device; calls may come from several
