@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int lim = p.causal ? min(p.Sk - 1, row + off) : p.Sk - 1;  // last key this row may see
     const int zk = b * p.Hkv + hkv;
     // FP8: per-tile dequantisation scalars; the largest V scale of the row block
-    float cq = 1.f, sv_ref = 1.f;
+    float cq = 1.f, sv_ref = 1.f, lsv_ref = 0.f, ks_next = 0.f, vs_next = 0.f;
     if constexpr (T::kFp8) {
       cq = __ldg(&p.q_scale[(size_t)bh * p.nqt + (q0 + i * BM) / BM]);
       float mv = 0.f;
@@ -338,6 +338,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
       sv_ref = fmaxf(mv, 1e-30f);
+      lsv_ref = __log2f(sv_ref);
+      // key tile j's K and V scales are loaded during tile j - 1, off the critical path
+      if (my_nkv > 0) {
+        ks_next = __ldg(&p.k_scale[(size_t)zk * p.nkt]);
+        vs_next = __ldg(&p.v_scale[(size_t)zk * p.nkt]);
+      }
     }
     float m_use = -CUDART_INF_F;  // running max in log2 units (moved lazily)
     float l = 0.f;                // running sum relative to m_use (gives the LSE)
@@ -347,8 +353,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int j = 0; ok && j < my_nkv; ++j) {
       float cj = p.scale_log2, e_off = T::kPre;
       if constexpr (T::kFp8) {
-        cj *= cq * __ldg(&p.k_scale[(size_t)zk * p.nkt + j]);
-        e_off += __log2f(fmaxf(__ldg(&p.v_scale[(size_t)zk * p.nkt + j]), 1e-30f) / sv_ref);
+        cj *= cq * ks_next;
+        e_off += __log2f(fmaxf(vs_next, 1e-30f)) - lsv_ref;
+        if (j + 1 < my_nkv) {
+          ks_next = __ldg(&p.k_scale[(size_t)zk * p.nkt + j + 1]);
+          vs_next = __ldg(&p.v_scale[(size_t)zk * p.nkt + j + 1]);
+        }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i], j & 1, p.wait_ns, p.err))) {
         ok = false;
