@@ -838,17 +838,17 @@ def main():
                                 "sample": f"{heads} full causal heads of the headline workload in {t:.1f} s: "
                                           f"the fp64 NumPy oracle on {cores} single-threaded worker processes, "
                                           f"one head each at a time"}
-    # last: one compact entry per leg, so every figure survives a cut of the line's head
+    # last: one short entry per leg, so every figure survives a cut of the line's head
     legs = {HEADLINE: head, **extras}
+    line["legs_fields"] = ["value", "unit", "roofline frac (measured peak)", "ms per step", "median SM MHz"]
     line["legs"] = {}
     for name, r in legs.items():
         if not isinstance(r, dict) or "value" not in r:
             line["legs"][name] = r
             continue
         c = leg_clk.get(name, {})
-        line["legs"][name] = {"value": round(r["value"], 1), "unit": r["unit"],
-                              "frac": round(r["roofline"]["frac"], 4), "ms": round(r["ms_per_step"], 4),
-                              "mhz": c.get("sm_mhz")}
+        line["legs"][name] = [round(r["value"], 1), r["unit"], round(r["roofline"]["frac"], 3),
+                              round(r["ms_per_step"], 4), c.get("sm_mhz")]
     print(json.dumps(line), flush=True)
 
 

@@ -410,6 +410,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   a.causal = causal ? 1 : 0;
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_bwd(a, tq, tk, tv, tdo, tdq, reinterpret_cast<cudaStream_t>(stream)));

@@ -61,7 +61,7 @@ struct Cfg {
   static constexpr int OFF_DS = OFF_DO + NS * TILE; // dS^T staging: 128 keys x 128 queries bf16
   static constexpr int OFF_LSE = OFF_DS + 2 * HALF;  // 128 x (LSE log2, Dvec) of the current item
   static constexpr int OFF_BAR = OFF_LSE + 128 * 2 * 4;
-  static constexpr int NBAR = 1 + 2 * NS + 5;
+  static constexpr int NBAR = 1 + 2 * NS + 6;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
   // M = 128; K-major A and B (S^T, dP^T)
@@ -89,7 +89,9 @@ struct Params {
   __nv_bfloat16 *dk, *dv;
   int B, Hq, Hkv, Sq, Sk, causal, g, nqt;
   float scale, scale_log2;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies and on the CTA's own tensor-core work
+  uint64_t wait_ns;     // waits of one warp role on another
+  int stall;            // test hook: the compute warps first wait for a signal nothing gives
   unsigned *err;
 };
 
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *q_full = bars + 1, *dq_staged = q_full + NS;
   uint64_t *st_full = dq_staged + NS, *p_ready = st_full + 1, *dq_full = p_ready + 1, *dq_free = dq_full + 1;
   uint64_t *done_bar = dq_free + 1;
+  uint64_t *never = done_bar + 1;  // test hook: no thread ever arrives on it
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
   const int nkt = (p.Sk + BN - 1) / BN;
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 256);
     mbar_init(done_bar, 1);
+    mbar_init(never, 1);
     mbar_init_fence();
   }
   tc_fence_before();
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         const int slot = r % NS;
-        if (!mbar_wait(&dq_staged[slot], (r / NS) & 1, p.timeout_ns, p.err)) {
+        if (!mbar_wait(&dq_staged[slot], (r / NS) & 1, p.wait_ns, p.err)) {
           ok = false;
           break;
         }
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int slot = it % NS;
         if (!mbar_wait(&q_full[slot], (it / NS) & 1, p.timeout_ns, p.err)) break;
         // TMEM [0,128) still holds the previous dQ until the compute warps have read it
-        if (it > 0 && !mbar_wait(dq_free, (it - 1) & 1, p.timeout_ns, p.err)) break;
+        if (it > 0 && !mbar_wait(dq_free, (it - 1) & 1, p.wait_ns, p.err)) break;
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T: K-major operands, 32 bytes of D per instruction
         const uint32_t so = slot * C::TILE;
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_ss(tmem + COL_DPT, sdesc_add(v_km, o), sdesc_add(do_k, o), C::IDESC_SS, kk > 0);
         }
         tc_commit(st_full);
-        if (!mbar_wait(p_ready, it & 1, p.timeout_ns, p.err)) break;
+        if (!mbar_wait(p_ready, it & 1, p.wait_ns, p.err)) break;
         tc_fence_after();
         // dV += P^T dO and dK += dS^T Q: A from TMEM (16 queries = 8 columns per
         // instruction), B = dO / Q MN-major (rows = queries)
@@ -330,15 +334,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       return half ? __ldg(&p.dvec[r]) : __ldg(&p.lse[r]) * 1.4426950408889634f;
     };
     float nval = item_value(0);
-    bool ok = true;
-    for (int it = 0; it < nitems; ++it) {
+    // test hook: wait for a signal nothing gives, so that this wait runs out
+    bool ok = !p.stall || named_barrier_and(1, 256, mbar_wait(never, 0, p.wait_ns, p.err));
+    for (int it = 0; ok && it < nitems; ++it) {
       const int q0 = (qt0 + it % nvis) * BM;
       named_barrier_sync(1, 256);  // every compute thread is done with the previous item's values
       (half ? s_dv : s_l2)[k] = nval;
       // st_full also orders this item after the previous dQ MMA (a commit
       // covers every earlier MMA), the last reader of the dS^T staging buffer;
       // the barrier publishes the staged values
-      if (!named_barrier_and(1, 256, mbar_wait(st_full, it & 1, p.timeout_ns, p.err))) {
+      if (!named_barrier_and(1, 256, mbar_wait(st_full, it & 1, p.wait_ns, p.err))) {
         ok = false;
         break;
       }
@@ -377,7 +382,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(p_ready);
       if (it + 1 < nitems) nval = item_value(it + 1);
       // ---- dQ_i = dS K is in TMEM [0, D): add scale * dQ_i (this warp's columns) into the accumulator
-      if (!named_barrier_and(1, 256, mbar_wait(dq_full, it & 1, p.timeout_ns, p.err))) {
+      if (!named_barrier_and(1, 256, mbar_wait(dq_full, it & 1, p.wait_ns, p.err))) {
         ok = false;
         break;
       }
@@ -499,6 +504,8 @@ cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
+  p.wait_ns = a.wait_ns;
+  p.stall = a.stall;
   p.err = a.err;
   if ((long)((a.Sk + BN - 1) / BN) * a.B * a.Hkv > 0x7fffffffL) return cudaErrorNotSupported;
   e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

@@ -83,7 +83,9 @@ struct BwdArgs {
   float *dvec;           // workspace [B, Hq, Sq]
   int B, Hq, Hkv, Sq, Sk, D, causal;
   float scale;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies and on a CTA's own tensor-core work
+  uint64_t wait_ns;     // waits of one warp role on another inside a CTA
+  int stall;            // test hook: the compute warps first wait for a signal nothing gives
   unsigned *err;
 };
 

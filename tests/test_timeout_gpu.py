@@ -70,3 +70,26 @@ def test_fp8_forward_wait_runs_out_then_next_call_is_correct():
     Or, Lr = oracle.attention(*deq)
     assert rel_rms(o.double().cpu().numpy(), Or) <= FP8_REL_RMS
     assert np.abs(lse.cpu().numpy() - Lr).max() <= 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_wait_runs_out_then_next_call_is_correct(causal):
+    """The same for the backward: its gradient warps stall, the tensor-core
+    issuer's wait for the probabilities runs out; at most two query tiles per
+    key tile (S = 256), so the Q / dO ring never waits for a freed slot."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_prefill(1, 2, 2, 256, 256, 128, seed=5)
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    do = workloads.to_bf16(np.random.default_rng(6).standard_normal((1, 2, 256, 128)).astype(np.float32)).to(DEV)
+    o, lse = eta.fwd(q, k, v, causal=causal)
+    assert eta.get_error() == 0
+    st = _stalled(lambda: eta.bwd(q, k, v, o, lse, do, causal=causal))
+    assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
+    assert eta.get_error() == 0
+    dq, dk, dv = eta.bwd(q, k, v, o, lse, do, causal=causal)
+    assert eta.get_error() == 0
+    refs = oracle.attention_backward(w["q"].double().numpy(), w["k"].double().numpy(), w["v"].double().numpy(),
+                                     do.double().cpu().numpy(), causal=causal)[:3]
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+        rel = np.linalg.norm(g.double().cpu().numpy() - r) / np.linalg.norm(r)
+        assert rel <= 1e-2, f"{name} after timeout: relative RMS {rel:.3g}"
