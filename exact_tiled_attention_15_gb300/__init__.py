@@ -10,9 +10,10 @@
 ``decode_multi``  T <= 16 query tokens per sequence (speculative verification) -> (O, LSE)
 ``fwd_fp8``  FP8 e4m3 prefill with one scale per 128x128 tile -> (O, LSE)
 ``rotate_quantize_fp8``  Hadamard rotation + per-tile e4m3 quantisation of its inputs
+``rotate_quantize_fp8_many``  the same for up to four tensors (Q, K, V) in one launch
 ``get_error``  synchronise and read (and clear) the device error word
 
 All of them call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import STATUS, AttnError, bwd, debug_stall_role_waits, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, fwd_host, fwd_host_workspace_bytes, get_error, lib, rotate_quantize_fp8, version  # noqa: F401
+from ._lib import STATUS, AttnError, bwd, debug_stall_role_waits, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, fwd_host, fwd_host_workspace_bytes, get_error, lib, rotate_quantize_fp8, rotate_quantize_fp8_many, version  # noqa: F401

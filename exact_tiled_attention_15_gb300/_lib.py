@@ -36,6 +36,7 @@ SIGNATURES = {
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_rotate_quantize_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "attn_rotate_quantize_fp8_many": (_I, [_P, _I, _P, _I, _P]),
     "attn_get_error": (_I, [_P]),
     "attn_debug_stall_role_waits": (None, [_I]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
@@ -393,6 +394,51 @@ def rotate_quantize_fp8(x, signs=None, codes=None, scales=None):
                                         _stream(x.device))
     _check(st, "attn_rotate_quantize_fp8")
     return codes, scales
+
+
+class QuantTensor(ctypes.Structure):
+    """attn_quant_tensor of include/attn.h."""
+    _fields_ = [("x", _P), ("codes", _P), ("scales", _P), ("B", _I), ("H", _I), ("S", _I), ("rotate", _I)]
+
+
+QUANT_MAX_TENSORS = 4
+
+
+def rotate_quantize_fp8_many(xs, signs=None, rotate=None, outs=None):
+    """rotate_quantize_fp8 of several bf16 [B,H,S,128] tensors in one launch.
+    rotate[i] (default: every tensor when signs is given) says whether xs[i] is
+    rotated with signs; outs[i] is a preallocated (codes, scales) pair or None.
+    Returns [(codes, scales), ...] in the order of xs."""
+    n = len(xs)
+    if not 1 <= n <= QUANT_MAX_TENSORS:
+        raise ValueError(f"between 1 and {QUANT_MAX_TENSORS} tensors")
+    rotate = [signs is not None] * n if rotate is None else [bool(r) for r in rotate]
+    if len(rotate) != n or (outs is not None and len(outs) != n):
+        raise ValueError("rotate and outs need one entry per tensor")
+    if any(rotate) and signs is None:
+        raise ValueError("a rotated tensor needs signs")
+    for i, x in enumerate(xs):
+        _need(x, f"xs[{i}]", torch.bfloat16, 4)
+        if x.device != xs[0].device:
+            raise ValueError(f"xs[{i}] must be on {xs[0].device}")
+        if x.shape[3] != 128:
+            raise ValueError(f"xs[{i}] must have D = 128")
+    dev = xs[0].device
+    if signs is not None:
+        _need_like(signs, "signs", torch.float32, (128,), dev)
+    descs = (QuantTensor * n)()
+    results = []
+    for i, x in enumerate(xs):
+        B, H, S, D = x.shape
+        c, sc = (None, None) if outs is None or outs[i] is None else outs[i]
+        c = _out(c, f"codes[{i}]", torch.uint8, (B, H, S, D), dev)
+        sc = _out(sc, f"scales[{i}]", torch.float32, (B, H, -(-S // 128), 1), dev)
+        descs[i] = QuantTensor(x.data_ptr(), c.data_ptr(), sc.data_ptr(), B, H, S, int(rotate[i]))
+        results.append((c, sc))
+    st = lib().attn_rotate_quantize_fp8_many(ctypes.cast(descs, _P), n, _ptr(signs if any(rotate) else None), 128,
+                                             _stream(dev))
+    _check(st, "attn_rotate_quantize_fp8_many")
+    return results
 
 
 def get_error(device=None) -> int:

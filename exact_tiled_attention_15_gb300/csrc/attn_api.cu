@@ -417,25 +417,81 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   return from_cuda(attn::launch_bwd(a, tq, tk, tv, tdo, tdq, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+// Host-side checks of one tensor of a rotate + quantise call (no CUDA call).
+attn_status check_quant_tensor(const void *x, const uint8_t *codes, const float *scales, int B, int H, int S) {
+  if (!x || !codes || !scales) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if ((int64_t)B * H > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;  // TMA plane coordinate
+  return ATTN_OK;
+}
+
+// Adds one checked tensor to the launch.
+attn_status add_quant_tensor(attn::QuantArgs &a, const void *x, uint8_t *codes, float *scales, int B, int H, int S,
+                             int rotate) {
+  const int i = a.n;
+  if (!make_tmap(&a.tmx[i], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, S, (uint64_t)B * H, 64, 128) ||
+      !make_tmap(&a.tmc[i], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, S, (uint64_t)B * H, 128, 128))
+    return ATTN_ERR_CUDA;
+  a.scales[i] = scales;
+  a.nts[i] = (S + 127) / 128;
+  a.rotate[i] = rotate ? 1 : 0;
+  a.first[i + 1] = a.first[i] + (long)a.nts[i] * B * H;
+  a.n = i + 1;
+  return ATTN_OK;
+}
+
+attn_status launch_quant(attn::QuantArgs &a, attn_stream_t stream) {
+  a.timeout_ns = kDefaultTimeoutNs;
+  a.err = error_word();
+  if (!a.err) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_rotate_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
 attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
                                      int S, int D, attn_stream_t stream) {
   attn::NvtxRange nvtx_range("attn_rotate_quantize_fp8");
-  if (!x || !codes || !scales) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || S < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
-      (signs && (reinterpret_cast<uintptr_t>(signs) & 3u)))
-    return ATTN_ERR_INVALID_ARG;
+  if (D < 1) return ATTN_ERR_INVALID_ARG;
+  if (signs && (reinterpret_cast<uintptr_t>(signs) & 3u)) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_quant_tensor(x, codes, scales, B, H, S);
+  if (st != ATTN_OK) return st;
   if (D != 128) return ATTN_ERR_UNSUPPORTED;
-  if ((int64_t)B * H > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;  // TMA plane coordinate
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
-  CUtensorMap tmx, tmc;
-  if (!make_tmap(&tmx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, (uint64_t)B * H, 64, 128) ||
-      !make_tmap(&tmc, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, S, (uint64_t)B * H, 128, 128))
-    return ATTN_ERR_CUDA;
-  unsigned *err = error_word();
-  if (!err) return ATTN_ERR_CUDA;
-  return from_cuda(attn::launch_rotate_quantize(tmx, tmc, scales, signs, B, H, S, kDefaultTimeoutNs, err,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+  attn::QuantArgs a{};
+  a.signs = signs;
+  st = add_quant_tensor(a, x, codes, scales, B, H, S, signs != nullptr);
+  if (st != ATTN_OK) return st;
+  return launch_quant(a, stream);
+}
+
+attn_status attn_rotate_quantize_fp8_many(const attn_quant_tensor *tensors, int n, const float *signs, int D,
+                                          attn_stream_t stream) {
+  attn::NvtxRange nvtx_range("attn_rotate_quantize_fp8_many");
+  if (!tensors || n < 1) return ATTN_ERR_INVALID_ARG;
+  if (n > ATTN_QUANT_MAX_TENSORS) return ATTN_ERR_UNSUPPORTED;
+  if (D < 1) return ATTN_ERR_INVALID_ARG;
+  bool any_rot = false;
+  for (int i = 0; i < n; ++i) any_rot |= tensors[i].rotate != 0;
+  if (any_rot && (!signs || (reinterpret_cast<uintptr_t>(signs) & 3u))) return ATTN_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const attn_quant_tensor &t = tensors[i];
+    const attn_status st = check_quant_tensor(t.x, t.codes, t.scales, t.B, t.H, t.S);
+    if (st != ATTN_OK) return st;
+  }
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
+  attn::QuantArgs a{};
+  a.signs = any_rot ? signs : nullptr;
+  for (int i = 0; i < n; ++i) {
+    const attn_quant_tensor &t = tensors[i];
+    attn_status st = add_quant_tensor(a, t.x, t.codes, t.scales, t.B, t.H, t.S, t.rotate);
+    if (st != ATTN_OK) return st;
+  }
+  return launch_quant(a, stream);
 }
 
 void attn_debug_stall_role_waits(int enable) { g_debug_stall.store(enable ? 1 : 0, std::memory_order_relaxed); }

@@ -94,10 +94,24 @@ struct BwdArgs {
 cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const CUtensorMap &tdq, cudaStream_t stream);
 
-// Hadamard rotation (signs != nullptr) + per-128x128-tile e4m3 quantisation of a
-// bf16 [B, H, S, 128] tensor: tmx maps x as [B*H, S, 128] bf16 (64 x 128 boxes),
-// tmc the codes as [B*H, S, 128] uint8 (128 x 128 boxes), both 128-byte swizzled.
-cudaError_t launch_rotate_quantize(const CUtensorMap &tmx, const CUtensorMap &tmc, float *scales, const float *signs,
-                                   int B, int H, int S, uint64_t timeout_ns, unsigned *err, cudaStream_t stream);
+// Hadamard rotation + per-128x128-tile e4m3 quantisation of up to
+// kQuantMaxTensors bf16 [B, H, S, 128] tensors in one launch.  Per tensor i:
+// tmx[i] maps x as [B*H, S, 128] bf16 (64 x 128 boxes), tmc[i] the codes as
+// [B*H, S, 128] uint8 (128 x 128 boxes), both 128-byte swizzled; its tiles are
+// the launch's tiles first[i] .. first[i+1] - 1, nts[i] per (b, h) matrix;
+// rotate[i] selects y = x H diag(signs) / sqrt(128) (else y = x).
+constexpr int kQuantMaxTensors = 4;
+struct QuantArgs {
+  CUtensorMap tmx[kQuantMaxTensors], tmc[kQuantMaxTensors];
+  float *scales[kQuantMaxTensors];
+  long first[kQuantMaxTensors + 1];
+  int nts[kQuantMaxTensors];
+  int rotate[kQuantMaxTensors];
+  int n;
+  const float *signs;  // [128] of +-1; read only when some rotate[i] is set
+  uint64_t timeout_ns;
+  unsigned *err;
+};
+cudaError_t launch_rotate_quantize(const QuantArgs &a, cudaStream_t stream);
 
 }  // namespace attn

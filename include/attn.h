@@ -266,6 +266,35 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
 attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scales, const float *signs, int B, int H,
                                      int S, int D, attn_stream_t stream);
 
+/* One tensor of attn_rotate_quantize_fp8_many (layouts as for attn_rotate_quantize_fp8). */
+typedef struct attn_quant_tensor {
+  const void *x;   /* [B, H, S, 128] bf16, 16-byte aligned, read */
+  uint8_t *codes;  /* [B, H, S, 128] e4m3 bytes, 16-byte aligned, written */
+  float *scales;   /* [B, H, ceil(S/128), 1] fp32, written */
+  int B, H, S;
+  int rotate; /* nonzero: y = x R with the call's signs; zero: y = x */
+} attn_quant_tensor;
+
+#define ATTN_QUANT_MAX_TENSORS 4
+
+/*
+ * attn_rotate_quantize_fp8_many -- attn_rotate_quantize_fp8 for up to
+ * ATTN_QUANT_MAX_TENSORS tensors in one launch, e.g. the three inputs of
+ * attn_fwd_fp8: Q and K rotated with the same signs (so Q K^T is unchanged),
+ * V not.  The tensors' tiles are shared out over one persistent grid, so the
+ * launch's fixed costs (start, ramp, drain) are paid once.
+ *   tensors  host array of n descriptors (read during the call only)
+ *   signs    [128] fp32 of +-1, device; may be NULL when no tensor rotates
+ *   D        head dimension (128 only)
+ * Results are identical to one attn_rotate_quantize_fp8 call per tensor.
+ * ATTN_ERR_INVALID_ARG for a NULL or misaligned pointer, a size < 1, n < 1 or
+ * a rotating tensor without signs; ATTN_ERR_UNSUPPORTED for n >
+ * ATTN_QUANT_MAX_TENSORS, D != 128 or B * H > 2^30.  Tensors must not
+ * overlap one another's outputs.
+ */
+attn_status attn_rotate_quantize_fp8_many(const attn_quant_tensor *tensors, int n, const float *signs, int D,
+                                          attn_stream_t stream);
+
 /*
  * attn_get_error -- synchronises `stream`, then returns and clears the device
  * error word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a bounded

@@ -168,3 +168,26 @@ def test_fwd_host_validation(lib):
     assert host(wsb=n - 1) == INVALID
     assert host(Hkv=3) == INVALID
     assert host(D=96, wsb=lib.attn_fwd_host_workspace_bytes(2, 32, 32, 4096, 4096, 96)) == UNSUPPORTED
+
+
+def test_rotate_quantize_many_validation(lib):
+    """The multi-tensor quantise call checks every descriptor on the host."""
+    T = _lib.QuantTensor
+
+    def many(items, n=None, signs=A, D=128):
+        arr = (T * max(1, len(items)))(*items)
+        return lib.attn_rotate_quantize_fp8_many(ctypes.cast(arr, ctypes.c_void_p), len(items) if n is None else n,
+                                                 p(signs), D, None)
+
+    good = T(A, A, A, 2, 4, 300, 1)
+    assert many([good], n=0) == INVALID
+    assert lib.attn_rotate_quantize_fp8_many(None, 1, p(A), 128, None) == INVALID
+    assert many([good] * 5) == UNSUPPORTED                    # more than ATTN_QUANT_MAX_TENSORS
+    assert many([good, T(0, A, A, 2, 4, 300, 0)]) == INVALID  # NULL input
+    assert many([good, T(A, A + 8, A, 2, 4, 300, 0)]) == INVALID  # codes not 16-byte aligned
+    assert many([good, T(A, A, A + 2, 2, 4, 300, 0)]) == INVALID  # scales not 4-byte aligned
+    assert many([good, T(A, A, A, 2, 0, 300, 0)]) == INVALID   # H < 1
+    assert many([good], signs=0) == INVALID                      # a rotated tensor needs signs
+    assert many([good], signs=A + 2) == INVALID
+    assert many([good], D=64) == UNSUPPORTED
+    assert many([T(A, A, A, 1 << 16, 1 << 15, 128, 0)], signs=0) == UNSUPPORTED  # B * H > 2^30
