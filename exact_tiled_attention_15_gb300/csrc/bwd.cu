@@ -49,6 +49,17 @@
 namespace attn {
 namespace bwd {
 
+// Register reallocation between warpgroups (every warp of the warpgroup
+// executes it): give back registers down to N, or take more up to N.
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 constexpr int BM = 128;          // query rows per Q tile
 constexpr int BN = 128;          // keys per CTA
 constexpr int NS = 2;            // Q / dO ring depth

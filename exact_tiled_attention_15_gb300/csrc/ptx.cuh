@@ -183,17 +183,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 
-// Register reallocation between warpgroups (every warp of the warpgroup
-// executes it): give back registers down to N, or take more up to N.
-template <uint32_t N>
-__device__ __forceinline__ void reg_dealloc() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void reg_alloc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ------------------------------------------------------------------ tcgen05
 // Tensor memory (TMEM): 128 lanes x 512 columns of 32-bit cells per SM.  An
 // address is (lane << 16) | column.  A warp may only touch the 32 lanes
