@@ -24,10 +24,9 @@
 //               accumulators;
 //   warps 2-9   two epilogue warpgroups taking alternate tiles: each thread
 //               reads its row of z from TMEM, y = z / sqrt(D) (y = z without
-//               rotation), the tile amax
-//               is reduced across the group, codes y * (1 / scale) are rounded
-//               by the e4m3 conversion into a swizzled shared-memory tile that
-//               a TMA store writes out.
+//               rotation), the tile amax is reduced across the group, codes
+//               y * (1 / scale) are rounded by the e4m3 conversion into a
+//               swizzled shared-memory tile that a TMA store writes out.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -53,7 +52,7 @@ constexpr int OFF_OUT = OFF_IN + NST * IN_TILE;   // e4m3 codes, one tile per gr
 constexpr int OFF_RED = OFF_OUT + NG * BOX;       // amax partials [NG][4]
 constexpr int OFF_BAR = OFF_RED + NG * 4 * 4;
 constexpr int NBAR = 2 * NST + 2 * NACC + 1;      // full, empty, acc_full, acc_empty, mma_done
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM base, tiles consumed by the MMA warp
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM base, tiles landed (seen by the MMA warp), loads issued
 constexpr int SMEM = OFF_MISC + 16 + 1024;        // + alignment slack
 constexpr uint32_t TMEM_COLS = NACC * DQ;
 // instruction descriptor: f32 accumulate, A and B bf16, both K-major, N = 128, M = 128
@@ -92,9 +91,9 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < NACC; ++a) {
-      mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrival per warp of the group
+    for (int k = 0; k < NACC; ++k) {
+      mbar_init(&acc_full[k], 1);
+      mbar_init(&acc_empty[k], 4);  // one arrival per warp of the group
     }
     mbar_init(mma_done, 1);
     mbar_init_fence();
