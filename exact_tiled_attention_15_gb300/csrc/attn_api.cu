@@ -378,7 +378,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Sq, D)) return ATTN_ERR_INVALID_ARG;
-  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Sq, (uint64_t)B * Hq, 64, 128) ||

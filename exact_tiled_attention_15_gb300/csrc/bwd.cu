@@ -397,21 +397,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------- dQ read-out
     // Warp w reads TMEM lanes 32*(w%4) .. +31 (query rows of the item's tile)
     // and stages scale * dQ_i as 128-row x 32-column fp32 boxes with the
-    // 128-byte swizzle in the item's Q / dO slot; the TMA thread adds them
+    // 128-byte swizzle in the item's Q / dO slot (the first half of the boxes
+    // over its Q tile, the second over its dO tile); the TMA thread adds them
     // into the accumulator.
-    static_assert(D == 128, "two 64-column halves of dQ");
+    static_assert(D == 64 || D == 128, "dQ is read out in 64-column pieces");
     const int quad = warp & 3;
     const int rq = quad * 32 + lane;
     const uint32_t taddr = tmem + ((quad * 32) << 16);
-    auto stage = [&](const uint32_t (&v)[64], int slot, int bx0) {
+    // boxes bx0 .. bx0 + nbox - 1 from v[32 * vb ..]
+    auto stage = [&](const uint32_t (&v)[64], int slot, int bx0, int nbox, int vb) {
 #pragma unroll
       for (int bx = 0; bx < 2; ++bx)
+        if (bx < nbox) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t *w = v + bx * 32 + 4 * j;
-          *reinterpret_cast<float4 *>(C::dq_box(smem, slot, bx0 + bx) + rq * 128 + ((j ^ (rq & 7)) << 4)) =
-              make_float4(__uint_as_float(w[0]) * p.scale, __uint_as_float(w[1]) * p.scale,
-                          __uint_as_float(w[2]) * p.scale, __uint_as_float(w[3]) * p.scale);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t *w = v + (vb + bx) * 32 + 4 * j;
+            *reinterpret_cast<float4 *>(C::dq_box(smem, slot, bx0 + bx) + rq * 128 + ((j ^ (rq & 7)) << 4)) =
+                make_float4(__uint_as_float(w[0]) * p.scale, __uint_as_float(w[1]) * p.scale,
+                            __uint_as_float(w[2]) * p.scale, __uint_as_float(w[3]) * p.scale);
+          }
         }
     };
     for (int it = 0; it < nitems; ++it) {
@@ -419,16 +423,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int slot = it % NS;
       uint32_t v[64];
-      tmem_ld64(taddr + COL_DQ, v);  // columns 0 .. 63, over the item's Q tile
-      stage(v, slot, 0);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&dq_half[2 * slot]);
-      tmem_ld64(taddr + COL_DQ + 64, v);  // columns 64 .. 127, over its dO tile
+      tmem_ld64(taddr + COL_DQ, v);  // columns 0 .. 63
+      if constexpr (D == 128) {
+        stage(v, slot, 0, 2, 0);  // over the item's Q tile
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dq_half[2 * slot]);
+        tmem_ld64(taddr + COL_DQ + 64, v);  // columns 64 .. 127, over its dO tile
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_free);  // the next item's dP^T may overwrite these columns
-      stage(v, slot, 2);
+      if constexpr (D == 64) {
+        stage(v, slot, 0, 1, 0);  // columns 0 .. 31 over the item's Q tile
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dq_half[2 * slot]);
+        stage(v, slot, 1, 1, 1);  // columns 32 .. 63 over its dO tile
+      } else {
+        stage(v, slot, 2, 2, 0);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&dq_half[2 * slot + 1]);
@@ -635,6 +649,7 @@ cudaError_t launch(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
 cudaError_t launch_bwd(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const CUtensorMap &tdq, cudaStream_t stream) {
   if (a.D == 128) return bwd::launch<128>(a, tq, tk, tv, tdo, tdq, stream);
+  if (a.D == 64) return bwd::launch<64>(a, tq, tk, tv, tdo, tdq, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -115,7 +115,7 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
  *   dq [B, Hq, Sq, D], dk/dv [B, Hkv, Sk, D] bf16 (written).  With GQA the
  *   gradient of a key/value head sums over its group's query heads.
  *   workspace >= attn_bwd_workspace_bytes(B, Hq, Sq, D), 256-byte aligned.
- *   D == 128 only.  causal, scale as for attn_fwd.
+ *   D in {64, 128}.  causal, scale as for attn_fwd.
  * dS and P enter the tensor-core products as bf16; dQ is accumulated in fp32.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,

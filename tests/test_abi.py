@@ -145,7 +145,7 @@ def test_bwd_validation(lib):
     assert bwd(ws=A + 64) == INVALID
     assert bwd(wsb=n - 1) == INVALID
     assert bwd(Hkv=3) == INVALID
-    assert bwd(D=64, wsb=lib.attn_bwd_workspace_bytes(1, 2, 128, 64)) == UNSUPPORTED
+    assert bwd(D=96, wsb=lib.attn_bwd_workspace_bytes(1, 2, 128, 96)) == UNSUPPORTED  # D in {64, 128}
 
 
 def test_fwd_host_validation(lib):

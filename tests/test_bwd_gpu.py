@@ -29,17 +29,17 @@ def check(g, ref, what):
     return rr
 
 
-def run(B, Hq, Hkv, Sq, Sk, causal, seed=0):
+def run(B, Hq, Hkv, Sq, Sk, causal, seed=0, D=128):
     import exact_tiled_attention_15_gb300 as eta
-    w = workloads.make_prefill(B, Hq, Hkv, Sq, Sk, 128, seed=seed)
-    do = workloads.to_bf16(np.random.default_rng(seed + 100).standard_normal((B, Hq, Sq, 128)).astype(np.float32))
+    w = workloads.make_prefill(B, Hq, Hkv, Sq, Sk, D, seed=seed)
+    do = workloads.to_bf16(np.random.default_rng(seed + 100).standard_normal((B, Hq, Sq, D)).astype(np.float32))
     q, k, v, dod = w["q"].to(DEV), w["k"].to(DEV), w["v"].to(DEV), do.to(DEV)
     o, lse = eta.fwd(q, k, v, causal=causal)
     dq, dk, dv = eta.bwd(q, k, v, o, lse, dod, causal=causal)
     assert eta.get_error() == 0
     dqr, dkr, dvr, _, _ = oracle.attention_backward(w["q"].double().numpy(), w["k"].double().numpy(),
                                                     w["v"].double().numpy(), do.double().numpy(), causal=causal)
-    tag = f"{Hq}/{Hkv} {Sq}x{Sk} causal={causal}"
+    tag = f"{Hq}/{Hkv} {Sq}x{Sk} D={D} causal={causal}"
     return (check(dq.double().cpu().numpy(), dqr, "dQ " + tag), check(dk.double().cpu().numpy(), dkr, "dK " + tag),
             check(dv.double().cpu().numpy(), dvr, "dV " + tag))
 
@@ -62,6 +62,14 @@ def test_bwd_unequal(Sq, Sk, causal):
     """With Sq > Sk causal, the first rows see no key (zero gradients), and key
     tiles no query sees get zero dK, dV."""
     run(1, 2, 1, Sq, Sk, causal, seed=Sq + Sk)
+
+
+@pytest.mark.parametrize("Hq,Hkv,Sq,Sk", [(2, 2, 384, 384), (4, 1, 200, 330), (2, 1, 300, 100)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_d64(Hq, Hkv, Sq, Sk, causal):
+    """Head dimension 64: one 64-column box per tile; dQ read out of TMEM in one
+    piece and staged as two 32-column boxes (over the item's Q and dO tiles)."""
+    run(1, Hq, Hkv, Sq, Sk, causal, seed=Sq + 7 * Hq + Hkv, D=64)
 
 
 def test_bwd_train_workload_two_heads():
