@@ -211,6 +211,8 @@ attn_status attn_decode(const void *q, const void *kcache, const void *vcache, c
   a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   const size_t rows = (size_t)B * Hq * a.nsplit;
@@ -267,6 +269,8 @@ attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_
   a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   const size_t rows = (size_t)B * Hq * a.nsplit;
@@ -312,6 +316,8 @@ attn_status attn_decode_multi(const void *q, const void *kcache, const void *vca
   a.nsplit = attn::decode_nsplit(Lmax, a.chunk);
   a.scale = scale;
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   const size_t rows = (size_t)B * Hq * T * a.nsplit;
@@ -445,6 +451,8 @@ attn_status add_quant_tensor(attn::QuantArgs &a, const void *x, uint8_t *codes, 
 
 attn_status launch_quant(attn::QuantArgs &a, attn_stream_t stream) {
   a.timeout_ns = kDefaultTimeoutNs;
+  a.wait_ns = role_wait_ns();
+  a.stall = debug_stall();
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_rotate_quantize(a, reinterpret_cast<cudaStream_t>(stream)));

@@ -63,7 +63,9 @@ struct Params {
   int nhpc;    // query heads per CTA: nhpc * T <= 16 MMA rows
   int causal;  // T > 1: token t sits at position L - T + t and sees keys <= it
   float scale_log2;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies
+  uint64_t wait_ns;     // waits of one warp role on another
+  int stall;            // test hook: the consumers first wait for a signal nothing gives
   unsigned *err;
 };
 
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint64_t *empty = full + NST;
   uint64_t *cbar = empty + NST;  // consumer-warp barrier (bounded, unlike bar.sync)
   int *s_fail = reinterpret_cast<int *>(cbar + 1);
+  uint64_t *never = cbar + 2;  // test hook: no thread ever arrives on it
 
   // one-dimensional grid: split fastest, then (KV head, head chunk), then sequence
   const long cta = blockIdx.x;
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(&empty[i], NCW);
     }
     mbar_init(cbar, NCW * 32);
+    mbar_init(never, 1);
     *s_fail = 0;
     mbar_init_fence();
   }
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         int issued = 0;
         for (int t = 0; t < nst; ++t) {
           const int slot = t % NST;
-          if (t >= NST && !mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.timeout_ns, p.err)) break;
+          if (t >= NST && !mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.wait_ns, p.err)) break;
           uint8_t *kt = smem + slot * C::STAGE_BYTES;
           uint8_t *vt = kt + C::TILE_BYTES;
           mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       int issued = 0;
       for (int t = 0; t < nst; ++t) {
         const int slot = t % NST;
-        if (t >= NST && !__all_sync(0xffffffffu, mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.timeout_ns, p.err)))
+        if (t >= NST && !__all_sync(0xffffffffu, mbar_wait(&empty[slot], ((t / NST) - 1) & 1, p.wait_ns, p.err)))
           break;
         uint8_t *kt = smem + slot * C::STAGE_BYTES;
         uint8_t *vt = kt + C::TILE_BYTES;
@@ -228,8 +232,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     return mbar_wait(cbar, (cphase++) & 1, p.timeout_ns, p.err);
   };
 
-  bool ok = true;
-  for (int t = 0; t < nst; ++t) {
+  // test hook: wait for a signal nothing gives, so that this wait runs out
+  bool ok = !p.stall || mbar_wait(never, 0, p.wait_ns, p.err);
+  for (int t = 0; ok && t < nst; ++t) {
     const int slot = t % NST;
     if (!mbar_wait(&full[slot], (t / NST) & 1, p.timeout_ns, p.err)) {
       ok = false;
@@ -440,6 +445,8 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = a.timeout_ns;
+  p.wait_ns = a.wait_ns;
+  p.stall = a.stall;
   p.err = a.err;
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);

@@ -44,7 +44,9 @@ struct DecodeArgs {
   int B, Hq, Hkv, Lmax, D, chunk, nsplit;
   int T, causal;  // query tokens per sequence; bottom-right causal mask among them
   float scale;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies
+  uint64_t wait_ns;     // waits of one warp role on another (producer <-> consumers)
+  int stall;            // test hook: the consumer warps first wait for a signal nothing gives
   unsigned *err;
 };
 
@@ -109,7 +111,9 @@ struct QuantArgs {
   int rotate[kQuantMaxTensors];
   int n;
   const float *signs;  // [128] of +-1; read only when some rotate[i] is set
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // waits on copies and on a CTA's own tensor-core work
+  uint64_t wait_ns;     // waits of one warp role on another inside a CTA
+  int stall;            // test hook: the epilogue warps first wait for a signal nothing gives
   unsigned *err;
 };
 cudaError_t launch_rotate_quantize(const QuantArgs &a, cudaStream_t stream);

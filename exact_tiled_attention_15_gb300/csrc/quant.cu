@@ -51,7 +51,7 @@ constexpr int OFF_IN = OFF_BI + IN_TILE;
 constexpr int OFF_OUT = OFF_IN + NST * IN_TILE;   // e4m3 codes, one tile per group
 constexpr int OFF_RED = OFF_OUT + NG * BOX;       // amax partials [NG][4]
 constexpr int OFF_BAR = OFF_RED + NG * 4 * 4;
-constexpr int NBAR = 2 * NST + 2 * NACC + 1;      // full, empty, acc_full, acc_empty, mma_done
+constexpr int NBAR = 2 * NST + 2 * NACC + 2;      // full, empty, acc_full, acc_empty, mma_done, never
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM base, tiles landed (seen by the MMA warp), loads issued
 constexpr int SMEM = OFF_MISC + 16 + 1024;        // + alignment slack
 constexpr uint32_t TMEM_COLS = NACC * DQ;
@@ -78,12 +78,13 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *full = bars, *empty = bars + NST, *acc_full = bars + 2 * NST, *acc_empty = acc_full + NACC;
   uint64_t *mma_done = acc_empty + NACC;
+  uint64_t *never = mma_done + 1;  // test hook: no thread ever arrives on it
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   float *s_red = reinterpret_cast<float *>(smem + OFF_RED);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long t0 = blockIdx.x, step = gridDim.x, ntiles = a.first[a.n];
   const int my_n = t0 < ntiles ? (int)((ntiles - 1 - t0) / step + 1) : 0;
-  const uint64_t timeout_ns = a.timeout_ns;
+  const uint64_t timeout_ns = a.timeout_ns, wait_ns = a.wait_ns;  // copies / own products; other roles
   unsigned *const err = a.err;
 
   if (tid == 0) {
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
       mbar_init(&acc_empty[k], 4);  // one arrival per warp of the group
     }
     mbar_init(mma_done, 1);
+    mbar_init(never, 1);
     mbar_init_fence();
     misc[1] = 0;  // tiles whose loads the MMA warp saw land
     misc[2] = 0;  // tiles whose loads the producer issued
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
       for (int i = 0; i < a.n; ++i) tma_prefetch_desc(&a.tmx[i]);
       for (int it = 0; it < my_n; ++it) {
         const int s = it % NST;
-        if (it >= NST && !mbar_wait(&empty[s], ((it / NST) + 1) & 1, timeout_ns, err)) break;
+        if (it >= NST && !mbar_wait(&empty[s], ((it / NST) + 1) & 1, wait_ns, err)) break;
         long lt;
         const int i = tensor_of(a, t0 + it * step, lt);
         const int z = (int)(lt / a.nts[i]), y = (int)(lt % a.nts[i]) * TR;
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
         const int s = it % NST, acc = it % NACC;
         if (!mbar_wait(&full[s], (it / NST) & 1, timeout_ns, err)) break;
         misc[1] = it + 1;
-        if (it >= NACC && !mbar_wait(&acc_empty[acc], ((it / NACC) + 1) & 1, timeout_ns, err)) break;
+        if (it >= NACC && !mbar_wait(&acc_empty[acc], ((it / NACC) + 1) & 1, wait_ns, err)) break;
         tc_fence_after();
         long lt;
         const uint64_t db = a.rotate[tensor_of(a, t0 + it * step, lt)] ? db_rot : db_id;
@@ -186,12 +188,14 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
     const bool leader = warp == WARP_EPI + 4 * g && lane == 0;
     uint8_t *out = smem + OFF_OUT + g * BOX;
     float *red = s_red + g * 4;
+    // test hook: wait for a signal nothing gives, so that this wait runs out
+    const bool go = !a.stall || __all_sync(0xffffffffu, mbar_wait(never, 0, wait_ns, err));
     for (int it = g; it < my_n; it += NG) {
       const int acc = it % NACC;
       long lt;
       const int ti = tensor_of(a, t0 + it * step, lt);
       const float ys = a.rotate[ti] ? kInvSqrtD : 1.f;  // y = z / sqrt(D) for a rotation, y = x otherwise
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it / NACC) & 1, timeout_ns, err));
+      bool ok = go && __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it / NACC) & 1, wait_ns, err));
       uint32_t v[128];
       float amax = 0.f;
       if (ok) {

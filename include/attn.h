@@ -306,11 +306,14 @@ attn_status attn_get_error(attn_stream_t stream);
 /*
  * attn_debug_stall_role_waits -- test hook for the failure path of the
  * pipelines (no page defines it).  Inside a CTA of the prefill forward
- * (attn_fwd, attn_fwd_fp8) and the backward (attn_bwd), warp roles wait on
- * one another (the softmax for the scores, the tensor-core issuer for the
- * probabilities, ...), each wait bounded in time.  With enable != 0, every
- * such call made afterwards first has its softmax (backward: gradient) warps
- * wait for a signal that nothing gives, and the bound of the waits between
+ * (attn_fwd, attn_fwd_fp8), the backward (attn_bwd), the rotate + quantise
+ * kernel (attn_rotate_quantize_fp8, _many) and the decode split kernel
+ * (attn_decode, _paged, _multi, _noalloc), warp roles wait on one another
+ * (the softmax for the scores, the tensor-core issuer for the probabilities,
+ * the producer for a freed stage, ...), each wait bounded in time.  With
+ * enable != 0, every such call made afterwards first has its softmax
+ * (backward: gradient; quantise: epilogue; decode: consumer) warps wait for a
+ * signal that nothing gives, and the bound of the waits between
  * roles is cut to 1 ms: those waits run out, the kernel records
  * ATTN_ERR_TIMEOUT (returned by the next attn_get_error()) and the outputs of
  * that call are invalid.  Waits for data copies and for a CTA's own

@@ -1,4 +1,5 @@
-"""The bounded waits inside the prefill pipelines, made to run out on purpose.
+"""The bounded waits inside the prefill, backward and quantise pipelines, made
+to run out on purpose.
 
 Inside a forward CTA the softmax warps wait for the scores and the tensor-core
 issuer waits for the probabilities.  With attn_debug_stall_role_waits the
@@ -93,3 +94,45 @@ def test_backward_wait_runs_out_then_next_call_is_correct(causal):
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
         rel = np.linalg.norm(g.double().cpu().numpy() - r) / np.linalg.norm(r)
         assert rel <= 1e-2, f"{name} after timeout: relative RMS {rel:.3g}"
+
+
+def test_quantise_wait_runs_out_then_next_call_is_correct():
+    """The rotate + quantise kernel: its epilogue warps stall, so no product's
+    accumulator is ever read out; at most four tiles per CTA, so neither the
+    input ring nor the accumulators ever wait for a freed slot."""
+    import exact_tiled_attention_15_gb300 as eta
+    from test_quant_gpu import check, signs_for
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 2, 300, 128)).astype(np.float32)
+    x[rng.random(x.shape) < 0.005] *= 50.0
+    xb = workloads.to_bf16(x)
+    signs = signs_for(9)
+    xd, sg = xb.to(DEV), torch.from_numpy(signs.astype(np.float32)).to(DEV)
+    st = _stalled(lambda: eta.rotate_quantize_fp8(xd, sg))
+    assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
+    assert eta.get_error() == 0
+    codes, scales = eta.rotate_quantize_fp8(xd, sg)
+    assert eta.get_error() == 0
+    check(xb, signs, codes.cpu(), scales.cpu(), "after timeout")
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_wait_runs_out_then_next_call_is_correct(T):
+    """The split decode: its consumer warps stall; each split covers at most a
+    few 64-key stages, and a producer that would need a freed stage gives up
+    after the same 1 ms, so every wait ends."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = workloads.make_decode(3, 8, 2, 128, 100, 600, seed=11 + T, T=None if T == 1 else T)
+    q, kc, vc, sl = (w[n].to(DEV) for n in ("q", "kcache", "vcache", "seqlens"))
+    call = (lambda: eta.decode(q, kc, vc, sl)) if T == 1 else (lambda: eta.decode_multi(q, kc, vc, sl))
+    st = _stalled(call)
+    assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
+    assert eta.get_error() == 0
+    o, lse = call()
+    assert eta.get_error() == 0
+    qn, kn, vn = (w[n].double().numpy() for n in ("q", "kcache", "vcache"))
+    if T == 1:
+        Or, Lr = oracle.decode(qn, kn, vn, w["seqlens"].numpy(), 1 / np.sqrt(128))
+    else:
+        Or, Lr = oracle.decode_multi(qn, kn, vn, w["seqlens"].numpy(), causal=True, scale=1 / np.sqrt(128))
+    check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what=f"decode T{T} after timeout")
