@@ -64,7 +64,12 @@ struct Bf16 {
   static constexpr bool kFp8 = false;
   static constexpr int kElem = 2;        // bytes per element
   static constexpr int kMmaK = 16;       // K elements per MMA instruction (32 bytes)
-  static constexpr float kThresh = 8.f;  // lazy-rescale threshold, log2 units
+  // Lazy-rescale threshold, log2 units: the running max moves (and O is
+  // rescaled) only when a tile's max exceeds it by more than this, so P stays
+  // <= 2^32 -- well inside bf16's range -- and l <= Sk * 2^32, l * |V| (the
+  // fp32 O accumulator) far below fp32's 2^128 for any plausible V.  Fewer
+  // rescales: under outlier keys the max jumps often by a few units.
+  static constexpr float kThresh = 32.f;
   static constexpr float kPre = 0.f;     // log2 of the probability pre-scale
   static constexpr uint32_t kTypeBits = (1u << 7) | (1u << 10);  // A and B bf16
 };
