@@ -72,6 +72,8 @@ struct Bf16 {
   static constexpr float kThresh = 32.f;
   static constexpr float kPre = 0.f;     // log2 of the probability pre-scale
   static constexpr uint32_t kTypeBits = (1u << 7) | (1u << 10);  // A and B bf16
+  // Commit o_full after every P.V (else only after each tile's last one).
+  static constexpr bool kOFullEachTile = true;
 };
 
 struct Fp8 {
@@ -81,6 +83,11 @@ struct Fp8 {
   static constexpr float kThresh = 4.f;
   static constexpr float kPre = 4.f;
   static constexpr uint32_t kTypeBits = 0u;  // A and B e4m3
+  // A commit costs ~71 cycles of the tensor pipe, and an FP8 key tile has
+  // only ~1024 cycles of products: the per-tile o_full commits are dropped.
+  // The O rescale of tile j needs P_i V_{j-1} landed, which S_i(j) implies
+  // (it was issued after it, and the softmax has waited for S_i(j)).
+  static constexpr bool kOFullEachTile = false;
 };
 
 template <class T, int D>
@@ -292,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < BN / T::kMmaK; ++kk)
           mma_pv<T>(tmem + C::col_o(i), tmem + C::col_s(i) + kk * 8, sdesc_add(dv, kk * T::kMmaK * 128), C::IDESC_PV,
                     (j > 0 || kk > 0));
-        tc_commit(&o_full[i]);
+        if (T::kOFullEachTile || j + 1 == nkv_t[i]) tc_commit(&o_full[i]);
         return true;
       };
       bool ok = mbar_wait(q_full, 0, p.timeout_ns, p.err) && mbar_wait(&k_full[0], 0, p.timeout_ns, p.err);
@@ -459,7 +466,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // Rescale O_i by alpha once P_{j-1} V_{j-1} has landed (warp-uniform).
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.wait_ns, p.err))) {
+        if (T::kOFullEachTile &&
+            !__all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.wait_ns, p.err))) {
           tmem_st_wait();  // no store of P may still be in flight when the CTA ends
           ok = false;
           break;
@@ -480,7 +488,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&p_full[i]);
     }
     // ---------------------------------------------------------- epilogue
-    if (ok && my_nkv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[i], (my_nkv - 1) & 1, p.wait_ns, p.err));
+    if (ok && my_nkv > 0)
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&o_full[i], T::kOFullEachTile ? (my_nkv - 1) & 1 : 0, p.wait_ns, p.err));
     if (ok) {
       tc_fence_after();
       const float out_scale = T::kFp8 ? sv_ref * fast_exp2(-T::kPre) : 1.f;
