@@ -18,7 +18,8 @@
 // GB300 mapping, one CTA = two 128-row Q tiles of one (batch, query head):
 //   warp 8      TMA producers (cp.async.bulk.tensor, 128-byte swizzle,
 //               mbarrier tx counts): lane 0 loads Q once and streams K_j
-//               into a 2-stage ring, lane 1 streams V_j into a 3-stage ring;
+//               into a 2-stage ring, lane 1 streams V_j into a 3-stage ring
+//               (FP8: 3 and 3, K slots handed back with the V slots);
 //   warp 9      MMA issuer (one thread): S_i = Q_i K_j^T with tcgen05.mma
 //               (both operands in shared memory, fp32 accumulator in TMEM),
 //               then O_i += P_i V_j with P_i read from TMEM.  Issue order
@@ -52,8 +53,6 @@ namespace fwd {
 constexpr int BM = 128;          // query rows per Q tile
 constexpr int BN = 128;          // keys per K/V tile
 constexpr int NQT = 2;           // Q tiles per CTA
-constexpr int NSK = 2;           // K ring depth
-constexpr int NSV = 3;           // V ring depth
 constexpr int HALF = 128 * 128;  // 128 rows x 128 bytes: one 128-byte-swizzled slab of a tile
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr int THREADS = 10 * 32;
@@ -74,6 +73,11 @@ struct Bf16 {
   static constexpr uint32_t kTypeBits = (1u << 7) | (1u << 10);  // A and B bf16
   // Commit o_full after every P.V (else only after each tile's last one).
   static constexpr bool kOFullEachTile = true;
+  static constexpr int kNSK = 2, kNSV = 3;  // K and V ring depths
+  // K slot j is handed back by the commit that releases V slot j (one key
+  // tile later than its own commit would), saving a commit per key tile;
+  // needs equal ring depths.
+  static constexpr bool kKRelByV = false;
 };
 
 struct Fp8 {
@@ -88,10 +92,17 @@ struct Fp8 {
   // The O rescale of tile j needs P_i V_{j-1} landed, which S_i(j) implies
   // (it was issued after it, and the softmax has waited for S_i(j)).
   static constexpr bool kOFullEachTile = false;
+  // For the same reason K slots go back with the V release: K_j is free once
+  // P_1 V_j is done (S_1(j) came before it).  Three stages of each keep the
+  // loads ahead (four measured no faster, 160 KB of shared memory).
+  static constexpr int kNSK = 3, kNSV = 3;
+  static constexpr bool kKRelByV = true;
 };
 
 template <class T, int D>
 struct Cfg {
+  static constexpr int NSK = T::kNSK, NSV = T::kNSV;
+  static_assert(!T::kKRelByV || NSK == NSV, "K released with V needs equal ring depths");
   static constexpr int NH = D * T::kElem / 128;  // 128-byte slabs per row
   static constexpr int TILE = NH * HALF;         // one 128 x D tile
   static constexpr int OFF_Q = 0;
@@ -144,6 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, Params p) {
   using C = Cfg<T, D>;
+  constexpr int NSK = C::NSK, NSV = C::NSV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -240,7 +252,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       int nk = 0;
       for (int j = 0; j < nkv; ++j) {
         const int slot = j % NSK;
-        if (j >= NSK && !mbar_wait(&k_empty[slot], ((j / NSK) - 1) & 1, p.timeout_ns, p.err)) break;
+        uint64_t *freed = T::kKRelByV ? &v_empty[slot] : &k_empty[slot];
+        if (j >= NSK && !mbar_wait(freed, ((j / NSK) - 1) & 1, p.timeout_ns, p.err)) break;
         mbar_arrive_expect_tx(&k_full[slot], C::TILE);
 #pragma unroll
         for (int h = 0; h < C::NH; ++h)
@@ -308,7 +321,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < NQT; ++i)
           if (nkv_t[i] > 0) issue_s(i, 0);
-        tc_commit(&k_empty[0]);
+        if (!T::kKRelByV) tc_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < nkv; ++j) {
         const bool next = j + 1 < nkv;
@@ -324,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_commit(&v_empty[j % NSV]);
         if (next) {
           if (j + 1 < nkv_t[1]) issue_s(1, j + 1);
-          tc_commit(&k_empty[(j + 1) % NSK]);
+          if (!T::kKRelByV) tc_commit(&k_empty[(j + 1) % NSK]);
         }
       }
       // every product issued above has completed before the CTA moves on
