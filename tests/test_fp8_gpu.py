@@ -58,6 +58,18 @@ def test_fp8_gqa_unequal(Sq, Sk, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_fp8_many_key_tiles_gqa(causal):
+    """17 key tiles (the last one ragged), query groups of 4: the three-stage
+    K and V rings wrap several times with K slots handed back by the V
+    release, and under the causal mask the two Q tiles of a CTA visit
+    different numbers of key tiles."""
+    w = workloads.make_fp8_prefill(1, 8, 2, 2100, 2100, 128, seed=21)
+    o, lse = gpu_fp8(w, causal)
+    Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
+    check(o, lse, Or, Lr, f"fp8 2100 GQA 8/2 causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_fp8_running_max_jump(causal):
     """As for bf16: later key tiles x60 make the running max jump past the
     exp2 range, so the accumulated O must be multiplied by an underflowed 0."""

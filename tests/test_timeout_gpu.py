@@ -58,17 +58,21 @@ def test_forward_wait_runs_out_then_next_call_is_correct(S, D, causal):
     check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what=f"after timeout S{S} D{D}")
 
 
-def test_fp8_forward_wait_runs_out_then_next_call_is_correct():
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_wait_runs_out_then_next_call_is_correct(causal):
+    """The FP8 instantiation signals differently (one O commit per Q tile, K
+    slots handed back with the V slots); two key tiles per CTA and three-stage
+    rings, so no producer ever waits for a freed slot."""
     import exact_tiled_attention_15_gb300 as eta
     w = workloads.make_fp8_prefill(1, 2, 2, 256, 256, 128, seed=3)
     t = [w[n].to(DEV) for n in ("q8", "k8", "v8", "q_scale", "k_scale", "v_scale")]
-    st = _stalled(lambda: eta.fwd_fp8(*t))
+    st = _stalled(lambda: eta.fwd_fp8(*t, causal=causal))
     assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
     assert eta.get_error() == 0
-    o, lse = eta.fwd_fp8(*t)
+    o, lse = eta.fwd_fp8(*t, causal=causal)
     assert eta.get_error() == 0
     deq = [oracle.dequantize_tiles(w[n + "8"].numpy(), w[n + "_scale"].numpy()) for n in ("q", "k", "v")]
-    Or, Lr = oracle.attention(*deq)
+    Or, Lr = oracle.attention(*deq, causal=causal)
     assert rel_rms(o.double().cpu().numpy(), Or) <= FP8_REL_RMS
     assert np.abs(lse.cpu().numpy() - Lr).max() <= 1e-3
 
