@@ -589,10 +589,10 @@ def run_quant(steps, warmup, flush, peaks):
     from exact_tiled_attention_15_gb300 import workloads
     cfg = workloads.WORKLOADS["fp8_prefill"]
     B, H, S, D = cfg["B"], cfg["Hq"], cfg["S"], cfg["D"]
-    w = workloads.make_prefill(B, H, H, S, S, D, seed=0)
+    w = workloads.make_workload("fp8_prefill", seed=0)  # bf16 draws with 0.5 % outliers x50, and the signs
     dev = torch.device("cuda")
     xs = [w[n].to(dev) for n in ("q", "k", "v")]
-    signs = torch.from_numpy(np.random.default_rng(0).integers(0, 2, D).astype(np.float32) * 2 - 1).to(dev)
+    signs = torch.from_numpy(w["signs"].astype(np.float32)).to(dev)
     outs = [(torch.empty(B, H, S, D, dtype=torch.uint8, device=dev),
              torch.empty(B, H, -(-S // 128), 1, dtype=torch.float32, device=dev)) for _ in range(3)]
 
@@ -628,7 +628,13 @@ def run_fp8(steps, warmup, flush, peaks):
     B, Hq, Hkv, S, D, causal = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["D"], cfg["causal"]
     w = workloads.make_workload(name, seed=0)
     dev = torch.device("cuda")
-    t = {n: w[n].to(dev) for n in ("q8", "k8", "v8", "q_scale", "k_scale", "v_scale")}
+    # the e4m3 inputs: Q and K rotated by the draw's signs, V not, by the library's quantise kernel
+    signs = torch.from_numpy(w["signs"].astype("float32")).to(dev)
+    (q8, qs), (k8, ks), (v8, vs) = eta.rotate_quantize_fp8_many([w[n].to(dev) for n in ("q", "k", "v")], signs,
+                                                                rotate=(True, True, False))
+    if eta.get_error() != 0:
+        raise RuntimeError("fp8 inputs: device-side error")
+    t = dict(q8=q8, k8=k8, v8=v8, q_scale=qs, k_scale=ks, v_scale=vs)
     o = torch.empty(B, Hq, S, D, device=dev, dtype=torch.bfloat16)
     lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
     fn = lambda: eta.fwd_fp8(t["q8"], t["k8"], t["v8"], t["q_scale"], t["k_scale"], t["v_scale"],  # noqa: E731

@@ -1,9 +1,9 @@
 """Seeded synthetic inputs for the attention kernels and for the CPU oracle.
 
-This module only draws and encodes inputs: it holds none of the attention
-arithmetic.  Both the CUDA path and the oracle receive exactly the tensors made
-here.  Rounding to bf16 and to e4m3 uses PyTorch's CPU casts (round to nearest
-even); the oracle decodes the resulting codes with its own decoder.
+This module only draws inputs: it holds none of the method's arithmetic (no
+attention, no rotation, no quantisation).  Both the CUDA path and the oracle
+receive exactly the tensors made here.  Rounding to bf16 uses PyTorch's CPU
+cast (round to nearest even).
 
 Recipe (every workload, seed 0 unless the caller passes another seed):
   * generator: NumPy ``default_rng(seed)`` (PCG64);
@@ -19,12 +19,8 @@ as in its §6.2 (h query heads, G key/value heads, h/G per group).
 """
 from __future__ import annotations
 
-import math
-
 import numpy as np
 import torch
-
-TILE = 128  # FP8 scale tile: one fp32 scale per 128 rows x 128 columns
 
 # Named workloads.  ``S`` is Sq = Sk for prefill.
 WORKLOADS = {
@@ -130,48 +126,16 @@ def make_paged_decode(B, Hq, Hkv, D, Lmin, Lmax, page_size, seed=0, poison=True,
                 kcache=w["kcache"], vcache=w["vcache"], page_size=page_size)
 
 
-def hadamard(n: int) -> np.ndarray:
-    """Sylvester Hadamard matrix of order n (a power of two), entries +-1."""
-    assert n > 0 and (n & (n - 1)) == 0
-    h = np.ones((1, 1), dtype=np.float64)
-    while h.shape[0] < n:
-        h = np.block([[h, h], [h, -h]])
-    return h
-
-
-def rotation(D: int, signs: np.ndarray) -> np.ndarray:
-    """Random orthogonal matrix R = H_D . diag(signs) / sqrt(D), float64."""
-    return hadamard(D) * signs[None, :].astype(np.float64) / math.sqrt(D)
-
-
-def quantize_tiles_e4m3(x: torch.Tensor, tile: int = TILE):
-    """Block quantisation: one fp32 scale per tile x tile block of each (b, h) matrix.
-
-    x: float32 [B, H, S, D].  scale = amax / 448 (1 where a block is all zero);
-    code = e4m3(x / scale), rounded to nearest even by PyTorch's cast.
-    Returns (codes uint8 [B,H,S,D], scales float32 [B,H,ceil(S/tile),ceil(D/tile)]).
-    """
-    B, H, S, D = x.shape
-    nt_s, nt_d = -(-S // tile), -(-D // tile)
-    pad = torch.zeros(B, H, nt_s * tile, nt_d * tile, dtype=torch.float32)
-    pad[:, :, :S, :D] = x
-    blocks = pad.view(B, H, nt_s, tile, nt_d, tile)
-    amax = blocks.abs().amax(dim=(3, 5))
-    scales = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
-    scaled = blocks / scales[:, :, :, None, :, None]
-    scaled = scaled.clamp(-448.0, 448.0)
-    codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8)
-    codes = codes.view(B, H, nt_s * tile, nt_d * tile)[:, :, :S, :D].contiguous()
-    return codes, scales.contiguous()
-
-
 def make_fp8_prefill(B, Hq, Hkv, Sq, Sk, D, seed=0, outlier_frac=0.005, outlier_mult=50.0):
-    """FP8 e4m3 inputs with one fp32 scale per 128 x 128 tile.
+    """The draws behind the FP8 e4m3 prefill inputs.
 
-    bf16 N(0,1) draws with ``outlier_frac`` of the entries of each of Q, K, V
-    multiplied by ``outlier_mult``; Q and K are then multiplied (as row vectors)
-    by one seeded rotation R = H_D diag(s) / sqrt(D) in float32, which leaves
-    Q K^T unchanged; V is not rotated.  All three are then block-quantised.
+    bf16 N(0,1) draws for Q, K, V with ``outlier_frac`` of the entries of each
+    multiplied by ``outlier_mult`` (before the bf16 rounding), then D random
+    signs (+-1, float64) for the rotation R = H_D diag(signs) / sqrt(D).  The
+    e4m3 codes and their one-fp32-scale-per-128x128-tile come from these by the
+    rotate + quantise step (Q and K rotated by the same R, V not): the library's
+    ``rotate_quantize_fp8_many`` kernel, or the CPU oracle's
+    ``rotate_quantize`` where a test needs inputs independent of the GPU.
     """
     rng = np.random.default_rng(seed)
     q = rng.standard_normal((B, Hq, Sq, D), dtype=np.float32)
@@ -180,14 +144,7 @@ def make_fp8_prefill(B, Hq, Hkv, Sq, Sk, D, seed=0, outlier_frac=0.005, outlier_
     for x in (q, k, v):
         _apply_outliers(rng, x, outlier_frac, outlier_mult)
     signs = rng.integers(0, 2, size=D).astype(np.float64) * 2.0 - 1.0
-    R = torch.from_numpy(rotation(D, signs).astype(np.float32))
-    qb, kb, vb = to_bf16(q).float(), to_bf16(k).float(), to_bf16(v).float()
-    qr = (qb.reshape(-1, D) @ R).reshape(qb.shape)
-    kr = (kb.reshape(-1, D) @ R).reshape(kb.shape)
-    q8, qs = quantize_tiles_e4m3(qr)
-    k8, ks = quantize_tiles_e4m3(kr)
-    v8, vs = quantize_tiles_e4m3(vb)
-    return dict(q8=q8, k8=k8, v8=v8, q_scale=qs, k_scale=ks, v_scale=vs, signs=signs)
+    return dict(q=to_bf16(q), k=to_bf16(k), v=to_bf16(v), signs=signs)
 
 
 def make_workload(name: str, seed: int = 0, **override):

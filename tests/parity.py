@@ -71,3 +71,20 @@ def rel_rms(o_gpu, o_ref) -> float:
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     return float(np.linalg.norm(o_gpu - o_ref) / np.linalg.norm(o_ref))
+
+
+def fp8_inputs(w):
+    """The FP8 prefill inputs of a ``workloads.make_fp8_prefill`` draw, made by
+    the oracle's rotate + quantise (Q and K rotated by the draw's signs, V
+    not; one fp32 scale per 128 x 128 tile), as CPU tensors keyed q8, k8, v8,
+    q_scale, k_scale, v_scale.  The GPU and the oracle then both consume these
+    codes and scales, so neither side's inputs come from the other."""
+    import torch
+
+    import oracle
+    out = {}
+    for n, signs in (("q", w["signs"]), ("k", w["signs"]), ("v", None)):
+        codes, scales, _ = oracle.rotate_quantize(w[n].double().numpy(), signs)
+        out[n + "8"] = torch.from_numpy(codes)
+        out[n + "_scale"] = torch.from_numpy(scales.astype(np.float32))
+    return out

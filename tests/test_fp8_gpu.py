@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from exact_tiled_attention_15_gb300 import workloads
-from parity import FP8_REL_RMS, LSE_ABS, rel_rms
+from parity import FP8_REL_RMS, LSE_ABS, fp8_inputs, rel_rms
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -42,7 +42,7 @@ def check(o, lse, Or, Lr, what):
 @pytest.mark.parametrize("S", [1, 128, 300, 1000])
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_shapes(S, causal):
-    w = workloads.make_fp8_prefill(1, 2, 2, S, S, 128, seed=S)
+    w = fp8_inputs(workloads.make_fp8_prefill(1, 2, 2, S, S, 128, seed=S))
     o, lse = gpu_fp8(w, causal)
     Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
     check(o, lse, Or, Lr, f"fp8 S={S} causal={causal}")
@@ -51,7 +51,7 @@ def test_fp8_shapes(S, causal):
 @pytest.mark.parametrize("Sq,Sk", [(100, 700), (700, 100)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_gqa_unequal(Sq, Sk, causal):
-    w = workloads.make_fp8_prefill(2, 4, 2, Sq, Sk, 128, seed=Sq)
+    w = fp8_inputs(workloads.make_fp8_prefill(2, 4, 2, Sq, Sk, 128, seed=Sq))
     o, lse = gpu_fp8(w, causal)
     Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
     check(o, lse, Or, Lr, f"fp8 {Sq}x{Sk} causal={causal}")
@@ -63,7 +63,7 @@ def test_fp8_many_key_tiles_gqa(causal):
     K and V rings wrap several times with K slots handed back by the V
     release, and under the causal mask the two Q tiles of a CTA visit
     different numbers of key tiles."""
-    w = workloads.make_fp8_prefill(1, 8, 2, 2100, 2100, 128, seed=21)
+    w = fp8_inputs(workloads.make_fp8_prefill(1, 8, 2, 2100, 2100, 128, seed=21))
     o, lse = gpu_fp8(w, causal)
     Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
     check(o, lse, Or, Lr, f"fp8 2100 GQA 8/2 causal={causal}")
@@ -79,8 +79,9 @@ def test_fp8_running_max_jump(causal):
     v = torch.from_numpy(rng.standard_normal((1, 2, 400, 128)).astype(np.float32))
     k[:, :, 128:] *= 60.0
     w = {}
-    for n, x in (("q", q), ("k", k), ("v", v)):
-        w[n + "8"], w[n + "_scale"] = workloads.quantize_tiles_e4m3(x)
+    for n, x in (("q", q), ("k", k), ("v", v)):  # quantised without rotation
+        codes, scales, _ = oracle.rotate_quantize(x.double().numpy(), None)
+        w[n + "8"], w[n + "_scale"] = torch.from_numpy(codes), torch.from_numpy(scales.astype(np.float32))
     o, lse = gpu_fp8(w, causal)
     Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
     check(o, lse, Or, Lr, f"fp8 max jump causal={causal}")
@@ -93,7 +94,7 @@ def test_fp8_full_size_whole_tensor():
     dequantised inputs; the oracle runs whole heads on a process pool."""
     from oracle import pool
     cfg = workloads.WORKLOADS["fp8_prefill"]
-    w = workloads.make_workload("fp8_prefill", seed=0)
+    w = fp8_inputs(workloads.make_workload("fp8_prefill", seed=0))
     o, lse = gpu_fp8(w, cfg["causal"])
     B, Hq = o.shape[0], o.shape[1]
     heads = [(b, h) for b in range(B) for h in range(Hq)]

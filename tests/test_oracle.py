@@ -353,7 +353,8 @@ def test_e4m3_decoder_matches_library_cast_and_spec_points():
 
 
 def test_dequantize_tiles_matches_library_and_scale_layout():
-    w = workloads.make_fp8_prefill(B=1, Hq=2, Hkv=2, Sq=300, Sk=300, D=128, seed=4)
+    from parity import fp8_inputs
+    w = fp8_inputs(workloads.make_fp8_prefill(B=1, Hq=2, Hkv=2, Sq=300, Sk=300, D=128, seed=4))
     codes, scales = w["q8"], w["q_scale"]
     assert scales.shape == (1, 2, 3, 1)
     ours = oracle.dequantize_tiles(codes.numpy(), scales.numpy())
@@ -401,17 +402,29 @@ def test_rotate_quantize_round_trip_and_tile_scales():
     np.testing.assert_array_equal(c0, oracle.e4m3_encode(x / np.repeat(s0, 128, 2)[:, :, :300]))
 
 
-# ---------------------------------------------------------------- input generator pins
 def test_rotation_is_orthogonal_and_preserves_scores():
     """Incoherent processing (FlashAttention-3): rotating Q and K by the same
-    orthogonal R leaves Q K^T unchanged."""
+    orthogonal R = H_D diag(s) / sqrt(D) leaves Q K^T unchanged."""
     signs = np.random.default_rng(0).integers(0, 2, 128) * 2.0 - 1.0
-    R = workloads.rotation(128, signs)
+    R = oracle.quant.hadamard(128) * signs[None, :] / np.sqrt(128)
     np.testing.assert_allclose(R @ R.T, np.eye(128), atol=1e-12)
     q, k = rand(50, 128, seed=38), rand(60, 128, seed=39)
     np.testing.assert_allclose((q @ R) @ (k @ R).T, q @ k.T, atol=1e-10)
-    H = workloads.hadamard(8)
+    H = oracle.quant.hadamard(8)
     np.testing.assert_array_equal(H @ H.T, 8 * np.eye(8))
+    _, _, y = oracle.rotate_quantize(np.stack([q, q])[None], signs)      # the same R inside rotate_quantize
+    np.testing.assert_allclose(y[0, 0], q @ R, atol=1e-12)
+
+
+# ---------------------------------------------------------------- input generator pins
+def test_fp8_draws_recipe():
+    """The FP8 draws: bf16 Q, K, V with about 0.5 % of the entries x50, and
+    D rotation signs of +-1; nothing is rotated or quantised here."""
+    w = workloads.make_fp8_prefill(B=1, Hq=2, Hkv=1, Sq=512, Sk=512, D=128, seed=0)
+    assert w["q"].dtype == torch.bfloat16 and w["q"].shape == (1, 2, 512, 128) and w["k"].shape == (1, 1, 512, 128)
+    assert set(np.unique(w["signs"])) == {-1.0, 1.0} and w["signs"].shape == (128,)
+    big = (w["q"].float().abs() > 8).float().mean().item()     # |N(0,1)| > 8 never happens without a x50
+    assert 0.002 < big < 0.008
 
 
 def test_decode_seqlens_recipe():

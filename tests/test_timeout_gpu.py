@@ -22,7 +22,7 @@ import torch
 
 import oracle
 from exact_tiled_attention_15_gb300 import workloads
-from parity import FP8_REL_RMS, check_bf16, rel_rms
+from parity import FP8_REL_RMS, check_bf16, fp8_inputs, rel_rms
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -64,7 +64,7 @@ def test_fp8_forward_wait_runs_out_then_next_call_is_correct(causal):
     slots handed back with the V slots); two key tiles per CTA and three-stage
     rings, so no producer ever waits for a freed slot."""
     import exact_tiled_attention_15_gb300 as eta
-    w = workloads.make_fp8_prefill(1, 2, 2, 256, 256, 128, seed=3)
+    w = fp8_inputs(workloads.make_fp8_prefill(1, 2, 2, 256, 256, 128, seed=3))
     t = [w[n].to(DEV) for n in ("q8", "k8", "v8", "q_scale", "k_scale", "v_scale")]
     st = _stalled(lambda: eta.fwd_fp8(*t, causal=causal))
     assert st == ATTN_ERR_TIMEOUT, eta.STATUS.get(st, st)
