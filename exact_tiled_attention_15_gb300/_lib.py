@@ -379,8 +379,8 @@ def fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, ret
 
 
 def rotate_quantize_fp8(x, signs=None, codes=None, scales=None):
-    """bf16 x [B,H,S,128] -> (e4m3 codes uint8 [B,H,S,128], scales fp32 [B,H,ceil(S/128),1]).
-    With signs ([128] float32 of +-1) the rows are first multiplied by H_128 diag(signs) / sqrt(128)."""
+    """bf16 x [B,H,S,D] -> (e4m3 codes uint8 [B,H,S,D], scales fp32 [B,H,ceil(S/128),1]), D = 64 or 128.
+    With signs ([D] float32 of +-1) the rows are first multiplied by H_D diag(signs) / sqrt(D)."""
     _need(x, "x", torch.bfloat16, 4)
     B, H, S, D = x.shape
     if signs is not None:
@@ -405,7 +405,7 @@ QUANT_MAX_TENSORS = 4
 
 
 def rotate_quantize_fp8_many(xs, signs=None, rotate=None, outs=None):
-    """rotate_quantize_fp8 of several bf16 [B,H,S,128] tensors in one launch.
+    """rotate_quantize_fp8 of several bf16 [B,H,S,D] tensors (one D, 64 or 128) in one launch.
     rotate[i] (default: every tensor when signs is given) says whether xs[i] is
     rotated with signs; outs[i] is a preallocated (codes, scales) pair or None.
     Returns [(codes, scales), ...] in the order of xs."""
@@ -421,11 +421,12 @@ def rotate_quantize_fp8_many(xs, signs=None, rotate=None, outs=None):
         _need(x, f"xs[{i}]", torch.bfloat16, 4)
         if x.device != xs[0].device:
             raise ValueError(f"xs[{i}] must be on {xs[0].device}")
-        if x.shape[3] != 128:
-            raise ValueError(f"xs[{i}] must have D = 128")
+        if x.shape[3] != xs[0].shape[3]:
+            raise ValueError(f"xs[{i}] must have the head dimension of xs[0]")
     dev = xs[0].device
+    D = int(xs[0].shape[3])
     if signs is not None:
-        _need_like(signs, "signs", torch.float32, (128,), dev)
+        _need_like(signs, "signs", torch.float32, (D,), dev)
     descs = (QuantTensor * n)()
     results = []
     for i, x in enumerate(xs):
@@ -435,7 +436,7 @@ def rotate_quantize_fp8_many(xs, signs=None, rotate=None, outs=None):
         sc = _out(sc, f"scales[{i}]", torch.float32, (B, H, -(-S // 128), 1), dev)
         descs[i] = QuantTensor(x.data_ptr(), c.data_ptr(), sc.data_ptr(), B, H, S, int(rotate[i]))
         results.append((c, sc))
-    st = lib().attn_rotate_quantize_fp8_many(ctypes.cast(descs, _P), n, _ptr(signs if any(rotate) else None), 128,
+    st = lib().attn_rotate_quantize_fp8_many(ctypes.cast(descs, _P), n, _ptr(signs if any(rotate) else None), D,
                                              _stream(dev))
     _check(st, "attn_rotate_quantize_fp8_many")
     return results

@@ -338,8 +338,10 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
        reinterpret_cast<uintptr_t>(v_scale)) & 3u)
     return ATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
-  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
+  // 128-column boxes: for D = 64 the upper 64 columns of a box lie outside the
+  // tensor and arrive as zeros
   CUtensorMap tq, tk, tv;
   if (!make_tmap(&tq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, Sq, (uint64_t)B * Hq, 128, 128) ||
       !make_tmap(&tk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, Sk, (uint64_t)B * Hkv, 128, 128) ||
@@ -435,11 +437,14 @@ attn_status check_quant_tensor(const void *x, const uint8_t *codes, const float 
 }
 
 // Adds one checked tensor to the launch.
+// For D = 64 the kernel still reads two 64-column slabs (the second lies
+// outside the tensor and arrives as zeros) and stores 128-column boxes of
+// codes, whose upper 64 columns lie outside the tensor and are dropped.
 attn_status add_quant_tensor(attn::QuantArgs &a, const void *x, uint8_t *codes, float *scales, int B, int H, int S,
-                             int rotate) {
+                             int D, int rotate) {
   const int i = a.n;
-  if (!make_tmap(&a.tmx[i], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, S, (uint64_t)B * H, 64, 128) ||
-      !make_tmap(&a.tmc[i], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128, S, (uint64_t)B * H, 128, 128))
+  if (!make_tmap(&a.tmx[i], x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, S, (uint64_t)B * H, 64, 128) ||
+      !make_tmap(&a.tmc[i], codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, S, (uint64_t)B * H, 128, 128))
     return ATTN_ERR_CUDA;
   a.scales[i] = scales;
   a.nts[i] = (S + 127) / 128;
@@ -467,11 +472,12 @@ attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scale
   if (signs && (reinterpret_cast<uintptr_t>(signs) & 3u)) return ATTN_ERR_INVALID_ARG;
   attn_status st = check_quant_tensor(x, codes, scales, B, H, S);
   if (st != ATTN_OK) return st;
-  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
   attn::QuantArgs a{};
   a.signs = signs;
-  st = add_quant_tensor(a, x, codes, scales, B, H, S, signs != nullptr);
+  a.d = D;
+  st = add_quant_tensor(a, x, codes, scales, B, H, S, D, signs != nullptr);
   if (st != ATTN_OK) return st;
   return launch_quant(a, stream);
 }
@@ -490,13 +496,14 @@ attn_status attn_rotate_quantize_fp8_many(const attn_quant_tensor *tensors, int 
     const attn_status st = check_quant_tensor(t.x, t.codes, t.scales, t.B, t.H, t.S);
     if (st != ATTN_OK) return st;
   }
-  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (!sm103_device()) return ATTN_ERR_NO_DEVICE;
   attn::QuantArgs a{};
   a.signs = any_rot ? signs : nullptr;
+  a.d = D;
   for (int i = 0; i < n; ++i) {
     const attn_quant_tensor &t = tensors[i];
-    attn_status st = add_quant_tensor(a, t.x, t.codes, t.scales, t.B, t.H, t.S, t.rotate);
+    attn_status st = add_quant_tensor(a, t.x, t.codes, t.scales, t.B, t.H, t.S, D, t.rotate);
     if (st != ATTN_OK) return st;
   }
   return launch_quant(a, stream);

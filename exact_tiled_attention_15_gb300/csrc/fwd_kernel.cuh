@@ -130,6 +130,7 @@ struct Params {
   float *lse;
   const float *q_scale, *k_scale, *v_scale;  // FP8 only
   int B, Hq, Hkv, Sq, Sk, causal, g, nqb, nqt, nkt;
+  int dout;  // columns of O (and its row stride): D, or 64 for FP8 inputs read as 128 columns
   int hc;  // (batch, head) pairs per launch-order chunk
   float scale_log2;
   uint64_t timeout_ns;  // waits on copies and on the CTA's own tensor-core work
@@ -199,9 +200,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x < NQT * BM) {
       const int row = q0 + threadIdx.x;
       if (row < p.Sq) {
-        uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + row) * D);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + row) * p.dout);
+        for (int c = 0; c < p.dout / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
         if (p.lse) p.lse[(size_t)bh * p.Sq + row] = -CUDART_INF_F;
       }
     }
@@ -508,9 +508,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const float out_scale = T::kFp8 ? sv_ref * fast_exp2(-T::kPre) : 1.f;
       const float inv = l_o > 0.f ? out_scale / l_o : 0.f;
-      uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + min(row, p.Sq - 1)) * D);
+      uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)bh * p.Sq + min(row, p.Sq - 1)) * p.dout);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
+        if (T::kFp8 && c * 32 >= p.dout) break;  // the zero columns of a 64-wide FP8 head
         uint32_t ov[32];
         if (my_nkv > 0) {
           tmem_ld32(taddr + o_col + c * 32, ov);
@@ -562,6 +563,7 @@ cudaError_t launch(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   p.nqt = (a.Sq + BM - 1) / BM;
   p.nkt = (a.Sk + BN - 1) / BN;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.dout = a.D;
   // chunks of (batch, head) pairs whose K and V take ~48 MB of L2, used when
   // the causal mask makes the lightest query block cost under half the
   // heaviest; otherwise all blocks cost about the same and the order stays

@@ -110,7 +110,8 @@ struct QuantArgs {
   int nts[kQuantMaxTensors];
   int rotate[kQuantMaxTensors];
   int n;
-  const float *signs;  // [128] of +-1; read only when some rotate[i] is set
+  int d;                // head dimension, 64 or 128 (a 64-wide tensor is read as 128 columns, the upper 64 zero)
+  const float *signs;  // [d] of +-1; read only when some rotate[i] is set
   uint64_t timeout_ns;  // waits on copies and on a CTA's own tensor-core work
   uint64_t wait_ns;     // waits of one warp role on another inside a CTA
   int stall;            // test hook: the epilogue warps first wait for a signal nothing gives

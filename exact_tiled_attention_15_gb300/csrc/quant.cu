@@ -14,7 +14,11 @@
 // core: z = x B with B = H_D diag(s) (entries +-1, exact in bf16; the identity
 // when there is no rotation), products exact, fp32 accumulation in TMEM.
 // One launch takes up to four tensors (e.g. Q and K rotated with the same
-// signs, V not); their tiles form one sequence that the CTAs split.
+// signs, V not); their tiles form one sequence that the CTAs split.  A head
+// dimension of 64 uses the same 128-column tiles: its upper 64 input columns
+// arrive from TMA as zeros, B keeps only its leading 64 x 64 block (H_64 is
+// the leading block of H_128), and the upper 64 columns of the codes fall
+// outside the output tensor map and are not stored.
 // Persistent, one CTA per SM, warp roles:
 //   warp 0      TMA producer: bf16 tiles into a four-stage shared-memory ring
 //               (two 64-column boxes, 128-byte swizzle = the K-major operand
@@ -37,7 +41,7 @@ namespace attn {
 namespace qnt {
 
 constexpr int TR = 128;    // rows per tile
-constexpr int DQ = 128;    // head dimension (one tile wide)
+constexpr int DQ = 128;    // columns of a tile: the head dimension (a 64-wide one is read with zeros above)
 constexpr int NST = 4;     // input ring depth (tiles)
 constexpr int NG = 2;      // epilogue warpgroups; group g takes the CTA's tiles g, g + NG, ...
 constexpr int NACC = 4;    // TMEM accumulators of 128 columns (two per group)
@@ -108,15 +112,21 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
   }
   // B^T[n][k] = s_n H[n][k] = s_n (-1)^popcount(n & k) (H is symmetric) for
   // the rotation, delta(n, k) for the identity; +-1 is 0x3f80 / 0xbf80 in bf16.
+  // For a.d = 64 only the 64 x 64 block n, k < 64 is nonzero (H_64 is the
+  // leading block of H_128): the zero upper columns of x add nothing and the
+  // upper columns of y come out zero.
   bool any_rot = false;
   for (int i = 0; i < a.n; ++i) any_rot |= a.rotate[i] != 0;
   if (tid < 2 * DQ) {
     const int n = tid % DQ;
     const bool rot = tid < DQ;
-    const uint32_t neg = rot && any_rot && __ldg(&a.signs[n]) < 0.f;
+    const int d = a.d;
+    const uint32_t neg = rot && any_rot && __ldg(&a.signs[n & (d - 1)]) < 0.f;
     uint8_t *bt = smem + (rot ? OFF_B : OFF_BI);
 #pragma unroll 1
     for (int c = 0; c < 16; ++c) {  // eight columns k = 8c .. 8c + 7
+      // outside the d x d block (d is 64 or 128, a multiple of 8): zero
+      const uint32_t keep = (n < d && 8 * c < d) ? 0xffffffffu : 0u;
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -126,7 +136,7 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
           const int k = 8 * c + 2 * e + i;
           h[i] = rot ? (0x3f80u | (((__popc(n & k) & 1u) ^ neg) << 15)) : (k == n ? 0x3f80u : 0u);
         }
-        w[e] = h[0] | (h[1] << 16);
+        w[e] = (h[0] | (h[1] << 16)) & keep;
       }
       *reinterpret_cast<uint4 *>(bt + (c >> 3) * BOX + sw(n, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -194,7 +204,8 @@ __global__ void __launch_bounds__(THREADS, 1) rotate_quantize_kernel(const __gri
       const int acc = it % NACC;
       long lt;
       const int ti = tensor_of(a, t0 + it * step, lt);
-      const float ys = a.rotate[ti] ? kInvSqrtD : 1.f;  // y = z / sqrt(D) for a rotation, y = x otherwise
+      // y = z / sqrt(d) for a rotation, y = x otherwise
+      const float ys = a.rotate[ti] ? (a.d == 64 ? 0.125f : kInvSqrtD) : 1.f;
       bool ok = go && __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (it / NACC) & 1, wait_ns, err));
       uint32_t v[128];
       float amax = 0.f;

@@ -239,7 +239,9 @@ attn_status attn_decode_noalloc(const void *q, const void *kcache, const void *v
  *   [B, Hkv, ceil(Sk/128), ceil(D/128)] fp32: the real value of element
  *   (b,h,s,d) is e4m3(code) * scale[b,h,s/128,d/128].
  *   o [B, Hq, Sq, D] bf16, lse [B, Hq, Sq] fp32 (may be NULL).
- *   D == 128 only (one scale tile spans the head dimension).
+ *   D = 64 or 128 (one scale tile spans the head dimension; D = 64 runs
+ *   on the D = 128 kernel with the upper 64 columns read as zeros, at the
+ *   D = 128 cost).  ATTN_ERR_UNSUPPORTED for any other D.
  * Scores are dequantised with one scalar per (query tile, key tile); the
  * probabilities enter the P.V product as e4m3 with the value tile's scale
  * folded in.
@@ -254,7 +256,7 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
  * rotation, then block quantisation to e4m3 with one fp32 scale per 128 x 128
  * tile ("FlashAttention scaling, multi-GPU training and weight quantization"
  * §1, FlashAttention-3: incoherent processing and block quantisation).
- *   x      [B, H, S, D] bf16 (D == 128 only)
+ *   x      [B, H, S, D] bf16, D = 64 or 128 (else ATTN_ERR_UNSUPPORTED)
  *   signs  [D] fp32 of +-1, or NULL for no rotation (use NULL for V and the
  *          same signs for Q and K, which leaves Q K^T unchanged)
  *   codes  [B, H, S, D] e4m3 bytes (written)
@@ -268,8 +270,8 @@ attn_status attn_rotate_quantize_fp8(const void *x, uint8_t *codes, float *scale
 
 /* One tensor of attn_rotate_quantize_fp8_many (layouts as for attn_rotate_quantize_fp8). */
 typedef struct attn_quant_tensor {
-  const void *x;   /* [B, H, S, 128] bf16, 16-byte aligned, read */
-  uint8_t *codes;  /* [B, H, S, 128] e4m3 bytes, 16-byte aligned, written */
+  const void *x;   /* [B, H, S, D] bf16, 16-byte aligned, read */
+  uint8_t *codes;  /* [B, H, S, D] e4m3 bytes, 16-byte aligned, written */
   float *scales;   /* [B, H, ceil(S/128), 1] fp32, written */
   int B, H, S;
   int rotate; /* nonzero: y = x R with the call's signs; zero: y = x */
@@ -284,12 +286,12 @@ typedef struct attn_quant_tensor {
  * V not.  The tensors' tiles are shared out over one persistent grid, so the
  * launch's fixed costs (start, ramp, drain) are paid once.
  *   tensors  host array of n descriptors (read during the call only)
- *   signs    [128] fp32 of +-1, device; may be NULL when no tensor rotates
- *   D        head dimension (128 only)
+ *   signs    [D] fp32 of +-1, device; may be NULL when no tensor rotates
+ *   D        head dimension of every tensor, 64 or 128
  * Results are identical to one attn_rotate_quantize_fp8 call per tensor.
  * ATTN_ERR_INVALID_ARG for a NULL or misaligned pointer, a size < 1, n < 1 or
  * a rotating tensor without signs; ATTN_ERR_UNSUPPORTED for n >
- * ATTN_QUANT_MAX_TENSORS, D != 128 or B * H > 2^30.  Tensors must not
+ * ATTN_QUANT_MAX_TENSORS, D not 64 or 128, or B * H > 2^30.  Tensors must not
  * overlap one another's outputs.
  */
 attn_status attn_rotate_quantize_fp8_many(const attn_quant_tensor *tensors, int n, const float *signs, int D,

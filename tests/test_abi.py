@@ -81,7 +81,8 @@ def test_fp8_rejects_bad_arguments_on_host(lib):
     assert fp8(lib, qs=0) == INVALID
     assert fp8(lib, qs=A + 2) == INVALID
     assert fp8(lib, Hq=4, Hkv=3) == INVALID
-    assert fp8(lib, D=64) == UNSUPPORTED
+    assert fp8(lib, D=96) == UNSUPPORTED  # D in {64, 128}
+    assert fp8(lib, D=256) == UNSUPPORTED
 
 
 def test_decode_workspace_and_validation(lib):
@@ -189,5 +190,5 @@ def test_rotate_quantize_many_validation(lib):
     assert many([good, T(A, A, A, 2, 0, 300, 0)]) == INVALID   # H < 1
     assert many([good], signs=0) == INVALID                      # a rotated tensor needs signs
     assert many([good], signs=A + 2) == INVALID
-    assert many([good], D=64) == UNSUPPORTED
+    assert many([good], D=96) == UNSUPPORTED  # D in {64, 128}
     assert many([T(A, A, A, 1 << 16, 1 << 15, 128, 0)], signs=0) == UNSUPPORTED  # B * H > 2^30

@@ -57,6 +57,20 @@ def test_fp8_gqa_unequal(Sq, Sk, causal):
     check(o, lse, Or, Lr, f"fp8 {Sq}x{Sk} causal={causal}")
 
 
+@pytest.mark.parametrize("Sq,Sk", [(300, 300), (100, 700), (700, 100)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_head_dim_64(Sq, Sk, causal):
+    """D = 64 on the D = 128 kernel: 128-column tiles whose upper half TMA
+    reads as zeros (nothing added to Q K^T, O's upper half zero); only the
+    64 real columns of O are written, at a row stride of 64."""
+    w = fp8_inputs(workloads.make_fp8_prefill(2, 4, 2, Sq, Sk, 64, seed=Sq + Sk))
+    assert w["q_scale"].shape == (2, 4, -(-Sq // 128), 1)
+    o, lse = gpu_fp8(w, causal)
+    assert o.shape == (2, 4, Sq, 64)
+    Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
+    check(o, lse, Or, Lr, f"fp8 D=64 {Sq}x{Sk} causal={causal}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_many_key_tiles_gqa(causal):
     """17 key tiles (the last one ragged), query groups of 4: the three-stage

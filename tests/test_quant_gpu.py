@@ -25,8 +25,8 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def signs_for(seed):
-    return np.random.default_rng(seed).integers(0, 2, 128).astype(np.float64) * 2 - 1
+def signs_for(seed, D=128):
+    return np.random.default_rng(seed).integers(0, 2, D).astype(np.float64) * 2 - 1
 
 
 def check(x_bf16, signs, codes_gpu, scales_gpu, what):
@@ -34,7 +34,8 @@ def check(x_bf16, signs, codes_gpu, scales_gpu, what):
     codes, scales, y = oracle.rotate_quantize(x, signs)
     # the transform's error bound (module docstring); then y = z / sqrt(D), 1 / scale
     # and y * (1 / scale) are each rounded once (3 half-ulps, rounded up to 4)
-    eps = 256 * 2.0 ** -24 * np.abs(x).sum(-1, keepdims=True) / np.sqrt(128) + 2.0 ** -22 * np.abs(y)
+    # (a 64-wide head is summed over 128 products too, half of them zero)
+    eps = 256 * 2.0 ** -24 * np.abs(x).sum(-1, keepdims=True) / np.sqrt(x.shape[-1]) + 2.0 ** -22 * np.abs(y)
     S = x.shape[2]
     pad = -S % 128
     eps_tile = np.pad(eps.max(-1), ((0, 0), (0, 0), (0, pad))).reshape(*x.shape[:2], -1, 128).max(-1)[..., None]
@@ -68,6 +69,29 @@ def test_rotate_quantize_shapes(S, rotate):
     codes, scales = eta.rotate_quantize_fp8(xb.to(DEV), sg)
     assert eta.get_error() == 0
     check(xb, signs, codes.cpu(), scales.cpu(), f"S={S} rotate={rotate}")
+
+
+@pytest.mark.parametrize("S", [300, 1000])
+@pytest.mark.parametrize("rotate", [True, False])
+def test_rotate_quantize_head_dim_64(S, rotate):
+    """D = 64: the kernel reads 128-column tiles whose upper half arrives as
+    zeros and rotates by H_64 diag(s) / 8, the leading block of its matrix;
+    only the 64 real columns of codes are stored."""
+    import exact_tiled_attention_15_gb300 as eta
+    rng = np.random.default_rng(S + 64)
+    x = rng.standard_normal((2, 3, S, 64)).astype(np.float32)
+    x[rng.random(x.shape) < 0.005] *= 50.0
+    xb = workloads.to_bf16(x)
+    signs = signs_for(S, 64) if rotate else None
+    sg = torch.from_numpy(signs.astype(np.float32)).to(DEV) if rotate else None
+    codes, scales = eta.rotate_quantize_fp8(xb.to(DEV), sg)
+    assert eta.get_error() == 0
+    assert codes.shape == (2, 3, S, 64) and scales.shape == (2, 3, -(-S // 128), 1)
+    check(xb, signs, codes.cpu(), scales.cpu(), f"D=64 S={S} rotate={rotate}")
+    many = eta.rotate_quantize_fp8_many([xb.to(DEV), xb.to(DEV)], sg if rotate else None, rotate=[rotate, False])
+    assert eta.get_error() == 0
+    assert torch.equal(many[0][0], codes) and torch.equal(many[0][1], scales)
+    check(xb, None, many[1][0].cpu(), many[1][1].cpu(), f"D=64 S={S} many, identity")
 
 
 def test_wide_dynamic_range_rows():
