@@ -91,3 +91,22 @@ def test_bwd_train_workload_two_heads():
         check(dq[sl].double().cpu().numpy(), dqr, f"dQ b{b} h{h}")
         check(dk[sl].double().cpu().numpy(), dkr, f"dK b{b} h{h}")
         check(dv[sl].double().cpu().numpy(), dvr, f"dV b{b} h{h}")
+
+
+def test_bwd_more_than_65535_head_pairs():
+    """66,000 (batch, KV head) pairs: the backward's grid (key tile, batch, KV
+    head) and its pre / post passes are one-dimensional; sampled heads at both
+    ends and in the middle against the oracle."""
+    import exact_tiled_attention_15_gb300 as eta
+    B, H, S, D = 2, 33000, 16, 64
+    w = workloads.make_prefill(B, H, H, S, S, D, seed=25)
+    do = workloads.to_bf16(np.random.default_rng(26).standard_normal((B, H, S, D)).astype(np.float32))
+    q, k, v = (w[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = eta.fwd(q, k, v, causal=True)
+    dq, dk, dv = eta.bwd(q, k, v, o, lse, do.to(DEV), causal=True)
+    assert eta.get_error() == 0
+    for b, h0 in ((0, 0), (1, 16496), (1, H - 8)):
+        part = [w[n][b:b + 1, h0:h0 + 8].double().numpy() for n in ("q", "k", "v")]
+        refs = oracle.attention_backward(*part, do[b:b + 1, h0:h0 + 8].double().numpy(), causal=True)[:3]
+        for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+            check(g[b:b + 1, h0:h0 + 8].double().cpu().numpy(), r, f"{name} 2x33000 heads b{b} h{h0}")

@@ -61,3 +61,22 @@ def test_decode_full_size_sampled():
         Or, Lr = oracle.decode(w["q"][b:b + 1].double().numpy(), w["kcache"][b:b + 1, :, :n].double().numpy(),
                                w["vcache"][b:b + 1, :, :n].double().numpy(), np.array([n]))
         check_bf16(o[b:b + 1], Or, lse[b:b + 1], Lr, what=f"decode full-size b={b}")
+
+
+def test_decode_more_than_65535_head_pairs():
+    """B * Hkv = 72,000 and B * Hq = 144,000: the split and combine grids are
+    one-dimensional; sampled heads at both ends and in the middle against the
+    oracle (query heads 2k, 2k + 1 read KV head k)."""
+    import exact_tiled_attention_15_gb300 as eta
+    B, Hq, Hkv, D = 2, 72000, 36000, 64
+    w = workloads.make_decode(B, Hq, Hkv, D, 1, 20, seed=24)
+    dev = torch.device("cuda:0")
+    o, lse = eta.decode(*(w[n].to(dev) for n in ("q", "kcache", "vcache", "seqlens")))
+    assert eta.get_error() == 0
+    for b, k0 in ((0, 0), (1, 17996), (1, Hkv - 8)):
+        q = w["q"][b:b + 1, 2 * k0:2 * k0 + 16].double().numpy()
+        kc = w["kcache"][b:b + 1, k0:k0 + 8].double().numpy()
+        vc = w["vcache"][b:b + 1, k0:k0 + 8].double().numpy()
+        Or, Lr = oracle.decode(q, kc, vc, w["seqlens"][b:b + 1].numpy(), 1 / np.sqrt(D))
+        check_bf16(o[b:b + 1, 2 * k0:2 * k0 + 16].double().cpu().numpy(), Or,
+                   lse[b:b + 1, 2 * k0:2 * k0 + 16].cpu().numpy(), Lr, what=f"decode 72000/36000 b{b} kv{k0}")

@@ -163,3 +163,19 @@ def test_chunked_prefill_full_size_whole_tensor():
     """A 512-token chunk against an 8192-key cache that holds it (B=8, 32/8
     heads, causal aligned at the bottom right): all 256 heads, every element."""
     _whole_tensor("chunked_prefill")
+
+
+def test_more_than_65535_head_pairs():
+    """66,000 (batch, head) pairs, beyond what a 16-bit grid dimension holds: the
+    launch folds (query block, batch, head) into grid x.  Head ranges at both
+    ends and in the middle of the batch match the oracle."""
+    import exact_tiled_attention_15_gb300 as eta
+    B, H, S, D = 2, 33000, 16, 64
+    w = workloads.make_prefill(B, H, H, S, S, D, seed=23)
+    o, lse = eta.fwd(*(w[n].to(DEV) for n in ("q", "k", "v")), causal=True)
+    assert eta.get_error() == 0
+    for b, h0 in ((0, 0), (1, 16496), (1, H - 8)):
+        part = {n: w[n][b:b + 1, h0:h0 + 8].double().numpy() for n in ("q", "k", "v")}
+        Or, Lr = oracle.attention(part["q"], part["k"], part["v"], causal=True)
+        check_bf16(o[b:b + 1, h0:h0 + 8].double().cpu().numpy(), Or, lse[b:b + 1, h0:h0 + 8].cpu().numpy(), Lr,
+                   what=f"fwd 2x33000 heads b{b} h{h0}")
