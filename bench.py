@@ -10,7 +10,10 @@ LSE fp32) on synthetic N(0,1) inputs; ``value`` is attention TFLOP/s
 carries the other workloads measured the same way (long-context GQA prefill,
 GQA decode KV-read GB/s, FP8 prefill TFLOP/s), each with its roofline
 fraction, plus the end-to-end figure through the public API with host
-buffers, and the CPU fp64 oracle timed on a bounded sample as a baseline.
+buffers (with whether its output equals the device-resident call's, bit for
+bit), and the CPU fp64 oracle timed on a bounded sample as a baseline; that
+sample's oracle outputs are also compared with the headline's GPU output on
+the same heads (``cpu_baseline.parity``).
 
 Timing: W warm-up steps, then K steps each bracketed by CUDA events on the
 launching stream, L2 flushed between steps outside the events (a 256 MB write,
@@ -359,6 +362,8 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0, leg="same"):
     ts = time_steps(fn, steps, warmup, flush, leg=name if leg == "same" else leg)
     if eta.get_error() != 0:
         raise RuntimeError(f"{name}: device-side error")
+    if name == HEADLINE:  # for the parity of the CPU baseline's sample
+        _GPU_OUT[name] = (o.cpu(), lse.cpu())
     flops = acc.prefill_flops(B, Hq, S, S, D, causal)
     ms = statistics.mean(ts)
     ach = flops / (ms * 1e-3) / 1e12
@@ -392,6 +397,9 @@ def run_prefill(name, steps, warmup, flush, peaks, e2e_steps=0, leg="same"):
                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q, k, v)),
                       "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4, "steps": len(te),
                       "api": "exact_tiled_attention_15_gb300.fwd_host (attn_fwd_host) on pinned host buffers"}
+        if name in _GPU_OUT:  # the same result as the device-resident call, bit for bit
+            res["e2e"]["equals_device_output"] = bool(torch.equal(ho, _GPU_OUT[name][0]) and
+                                                      torch.equal(hl, _GPU_OUT[name][1]))
         del ws
     del q, k, v, o, lse
     return res
@@ -663,6 +671,29 @@ def run_fp8(steps, warmup, flush, peaks):
 
 # ---------------------------------------------------------------- CPU oracle
 _INPUT_CACHE = {}
+_GPU_OUT = {}  # workload -> (O, LSE) of its last timed GPU step, on the host
+
+
+def sample_parity(name, heads, O, L):
+    """The timed run's GPU output against the oracle's on the sampled (b, h)
+    heads: max |dO| element by element, graded against 1e-2 plus half a bf16
+    ulp of the oracle's O (the output's own rounding), and max |dLSE| against
+    1e-3; None if the workload's output was not kept."""
+    import numpy as np
+    if name not in _GPU_OUT:
+        return None
+    o, lse = _GPU_OUT[name]
+    go = np.stack([o[b, h].double().numpy() for b, h in heads])
+    gl = np.stack([lse[b, h].double().numpy() for b, h in heads])
+    d = np.abs(go - O)
+    ax = np.abs(O)
+    half_ulp = np.where(ax > 0, np.exp2(np.floor(np.log2(np.where(ax > 0, ax, 1.0))) - 8), 0.0)
+    fin = np.isfinite(L)
+    same_inf = bool((np.isneginf(gl) == np.isneginf(L)).all())
+    dl = float(np.abs(gl[fin] - L[fin]).max()) if fin.any() else 0.0
+    return {"heads": len(heads), "elements": int(d.size), "max_abs_dO": float(d.max()),
+            "elements_over_1e-2": int((d > 1e-2).sum()), "max_abs_dLSE": dl,
+            "within_bound": bool((d <= 1e-2 + half_ulp).all() and dl <= 1e-3 and same_inf)}
 
 
 def oracle_head_sample(name, budget_s=10.0, max_heads=None):
@@ -700,7 +731,7 @@ def oracle_pool_sample(name, budget_s=10.0):
     one single-threaded worker per host core (heads are independent problems):
     after one untimed round (one head per worker, which also starts them),
     rounds of one head per worker until budget_s has elapsed.  Returns
-    (TFLOP/s, heads, seconds, workers, flops)."""
+    (TFLOP/s, heads, seconds, workers, flops, last round's heads, their O, LSE)."""
     from exact_tiled_attention_15_gb300 import accounting as acc, workloads
     from oracle.pool import HeadPool
     cfg = workloads.WORKLOADS[name]
@@ -713,15 +744,16 @@ def oracle_pool_sample(name, budget_s=10.0):
         n = pool.workers
         pool.run(order[:n], causal, 1.0 / math.sqrt(D))
         done, t, r = 0, 0.0, 1
+        batch, O, L = [], None, None
         while t < budget_s:
             batch = [order[(r * n + i) % len(order)] for i in range(n)]
             t0 = time.perf_counter()
-            pool.run(batch, causal, 1.0 / math.sqrt(D))
+            O, L = pool.run(batch, causal, 1.0 / math.sqrt(D))
             t += time.perf_counter() - t0
             done += n
             r += 1
     flops = acc.prefill_flops(1, done, S, S, D, causal)
-    return flops / t / 1e12, done, t, n, flops
+    return flops / t / 1e12, done, t, n, flops, batch, O, L
 
 
 def headline_config(ws):
@@ -849,7 +881,7 @@ def main():
         "e2e": None if e2e is None else {
             "value": e2e["value"] * ws, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
             "d2h_bytes_per_step": e2e["d2h_bytes_per_step"], "ms_per_step": e2e["ms_per_step"],
-            "api": e2e["api"]},
+            "api": e2e["api"], "equals_device_output": e2e.get("equals_device_output")},
         "gpu_launches": head["gpu_launches"],
         "clocks": {"sm_mhz": head_clk.get("sm_mhz") or clk["sm_mhz"],
                    "sm_max_mhz": getattr(nvml, "sm_max", None) or clk["sm_max_mhz"], "reasons": reasons,
@@ -861,11 +893,12 @@ def main():
         "timed_region_s": region_s,
     }
     if not args.no_cpu_baseline and ws == 1:
-        v, heads, t, cores, _ = oracle_pool_sample(HEADLINE, budget_s=10.0)
+        v, heads, t, cores, _, last, Oref, Lref = oracle_pool_sample(HEADLINE, budget_s=10.0)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{heads} full causal heads of the headline workload in {t:.1f} s: "
                                           f"the fp64 NumPy oracle on {cores} single-threaded worker processes, "
-                                          f"one head each at a time"}
+                                          f"one head each at a time",
+                                "parity": sample_parity(HEADLINE, last, Oref, Lref)}
     # last: one short entry per leg, so every figure survives a cut of the line's head
     legs = {HEADLINE: head, **extras}
     line["legs_fields"] = ["value", "unit", "roofline frac (measured peak)", "ms per step", "median SM MHz"]

@@ -56,3 +56,31 @@ def test_single_rank_aggregate():
     import bench
     assert bench.max_over_ranks(1.25, 1) == 1.25
     assert bench.whole_job_tflops(549.755813888e9, 1, 0.5) == pytest.approx(1099.5, rel=1e-4)
+
+
+def test_bench_sample_parity_grades_like_the_tests():
+    """bench.sample_parity: 1e-2 plus half a bf16 ulp of the oracle's O, and
+    1e-3 on the LSE; a kept GPU output is compared head by head."""
+    import numpy as np
+    import torch
+    import bench
+    rng = np.random.default_rng(0)
+    O = rng.standard_normal((2, 5, 4)) * 3
+    L = rng.standard_normal((2, 5))
+    L[1, 4] = -np.inf
+    o = torch.zeros(1, 3, 5, 4, dtype=torch.float64)
+    lse = torch.zeros(1, 3, 5, dtype=torch.float64)
+    heads = [(0, 2), (0, 0)]
+    for i, (b, h) in enumerate(heads):
+        o[b, h] = torch.from_numpy(O[i] + 0.009)
+        lse[b, h] = torch.from_numpy(L[i] + 5e-4)
+    bench._GPU_OUT["t"] = (o, lse)
+    try:
+        r = bench.sample_parity("t", heads, O, L)
+        assert r["within_bound"] and r["heads"] == 2 and r["elements_over_1e-2"] == 0
+        assert abs(r["max_abs_dO"] - 0.009) < 1e-12 and abs(r["max_abs_dLSE"] - 5e-4) < 1e-12
+        o[0, 0, 0, 0] += 0.05  # beyond 1e-2 + half an ulp of |O| < 16
+        assert not bench.sample_parity("t", heads, O, L)["within_bound"]
+        assert bench.sample_parity("absent", heads, O, L) is None
+    finally:
+        bench._GPU_OUT.pop("t", None)
