@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libattn.so")
 
 ATTN_OK = 0
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
-          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_NO_DEVICE", 6: "ATTN_ERR_SCRATCH_LIMIT"}
+          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_NO_DEVICE", 6: "ATTN_ERR_SCRATCH_LIMIT", 7: "ATTN_ERR_BAD_INDEX"}
+ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_INDEX = 4, 7  # device-side errors that get_error() reports
 
 # Every symbol the header declares, with (restype, argtypes).
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t

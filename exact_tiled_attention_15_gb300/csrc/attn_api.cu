@@ -124,6 +124,7 @@ const char *attn_status_str(attn_status s) {
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE";
     case ATTN_ERR_SCRATCH_LIMIT: return "ATTN_ERR_SCRATCH_LIMIT";
+    case ATTN_ERR_BAD_INDEX: return "ATTN_ERR_BAD_INDEX";
   }
   return "ATTN_ERR_UNKNOWN";
 }
@@ -256,6 +257,7 @@ attn_status attn_decode_paged(const void *q, const void *k_pages, const void *v_
   a.block_table = block_table;
   a.max_blocks = max_blocks;
   a.page_size = page_size;
+  a.num_pages = num_pages;
   a.o = o;
   a.lse = lse;
   a.B = B;

@@ -31,6 +31,9 @@
 namespace attn {
 namespace dec {
 
+// Device error word code of an out-of-range device-resident index (a
+// sequence length or a block-table entry): ATTN_ERR_BAD_INDEX of attn.h.
+constexpr unsigned kErrBadIndex = 7u;
 constexpr int KS = 64;                      // keys per pipeline stage
 constexpr int NST = 3;                      // pipeline stages
 constexpr int NCW = 4;                      // consumer warps, 16 keys of a stage each
@@ -55,7 +58,7 @@ struct Params {
   const __nv_bfloat16 *q;
   const int32_t *seqlens;
   const int32_t *block_table;  // paged cache only: [B, max_blocks]
-  int max_blocks, page_size, box_rows;
+  int max_blocks, page_size, box_rows, num_pages;
   float *part_o;
   float *part_lse;
   int B, Hq, Hkv, Lmax, chunk, nsplit, g, nhc;
@@ -100,7 +103,11 @@ __global__ void __launch_bounds__(THREADS, 2)
   // The merge kernel may be scheduled as soon as every CTA of this grid has
   // started; it waits for this grid's results before reading them.
   griddep_launch_dependents();
-  const int L = max(0, min(p.seqlens[b], p.Lmax));
+  const int seq_len = p.seqlens[b];
+  const int L = max(0, min(seq_len, p.Lmax));
+  // a length outside [0, Lmax] is clamped; one CTA per sequence reports it
+  if ((seq_len < 0 || seq_len > p.Lmax) && split == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0)
+    record_error(p.err, kErrBadIndex);
   const int s0 = split * p.chunk;
   if (s0 >= L) return;  // the whole CTA leaves together, before any barrier
   const int s1 = min(s0 + p.chunk, L);
@@ -157,6 +164,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       const int32_t *table = p.block_table + (size_t)b * p.max_blocks;
       int win = -1, entry = 0;  // entries win .. win+31 of the table, one per lane
+      bool bad = false;         // this lane met a live entry outside the pool
       int issued = 0;
       for (int t = 0; t < nst; ++t) {
         const int slot = t % NST;
@@ -174,6 +182,11 @@ __global__ void __launch_bounds__(THREADS, 2)
             if (win < 0 || blk >= win + 32) {
               win = blk;
               entry = (blk + lane < p.max_blocks) ? __ldg(&table[blk + lane]) : 0;
+              // an entry outside the pool is read as page 0; if this sequence
+              // reads it, that is reported once the copies are issued
+              const bool out = (unsigned)entry >= (unsigned)p.num_pages;
+              bad |= out && (blk + lane) * p.page_size < L;
+              entry = out ? 0 : entry;
             }
             page = __shfl_sync(0xffffffffu, entry, blk - win);
           }
@@ -188,6 +201,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
         issued = t + 1;
       }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kErrBadIndex);
       if (lane == 0)
         for (int t = max(0, issued - NST); t < issued; ++t)
           mbar_wait(&full[t % NST], (t / NST) & 1, p.timeout_ns, p.err);
@@ -429,6 +443,7 @@ cudaError_t launch(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMa
   p.block_table = a.block_table;
   p.max_blocks = a.max_blocks;
   p.page_size = a.page_size;
+  p.num_pages = a.num_pages;
   p.box_rows = a.page_size < KS ? a.page_size : KS;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;

@@ -36,7 +36,7 @@ struct DecodeArgs {
   const void *q;
   const int32_t *seqlens;
   const int32_t *block_table;  // nullptr: contiguous cache; else [B, max_blocks] page ids
-  int max_blocks, page_size;
+  int max_blocks, page_size, num_pages;
   void *o;
   float *lse;
   float *part_o;    // [B, Hq, nsplit, D]

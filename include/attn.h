@@ -57,7 +57,8 @@ typedef enum {
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
   ATTN_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (reported by attn_get_error) */
   ATTN_ERR_NO_DEVICE = 5,   /* no usable sm_103 device for this call */
-  ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_decode_noalloc: sizes need more than its fixed scratch */
+  ATTN_ERR_SCRATCH_LIMIT = 6, /* attn_decode_noalloc: sizes need more than its fixed scratch */
+  ATTN_ERR_BAD_INDEX = 7      /* a decode read a device-resident index out of range (reported by attn_get_error) */
 } attn_status;
 
 /*
@@ -137,7 +138,9 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int D);
  *   kcache, vcache [B, Hkv, Lmax, D] bf16
  *   seqlens [B] int32 device array, 0 <= seqlens[b] <= Lmax; rows at or beyond
  *           seqlens[b] are never read into the result.  seqlens[b] == 0 gives
- *           O = 0, LSE = -inf.  Values outside [0, Lmax] are clamped.
+ *           O = 0, LSE = -inf.  A value outside [0, Lmax] is clamped into it
+ *           and recorded as ATTN_ERR_BAD_INDEX for attn_get_error (that
+ *           sequence's output is then meaningless; the others are unaffected).
  *   lse     [B, Hq] fp32 natural-log LSE (may be NULL)
  *   workspace: device scratch of at least attn_decode_workspace_bytes(...)
  *           bytes, 256-byte aligned; contents on entry do not matter; calls that
@@ -187,8 +190,9 @@ attn_status attn_decode_multi(const void *q, const void *kcache, const void *vca
  *   block_table [B, max_blocks] int32: position t of sequence b is row
  *           t % page_size of page block_table[b, t / page_size].  Only the
  *           entries covering positions < seqlens[b] are read; an entry
- *           outside [0, num_pages) reads zeros (no fault) and gives a wrong
- *           but finite result for that sequence.
+ *           outside [0, num_pages) is read as page 0 (no fault) and recorded
+ *           as ATTN_ERR_BAD_INDEX for attn_get_error (that sequence's output is
+ *           then meaningless; the others are unaffected).
  *   seqlens [B] int32, 0 <= seqlens[b] <= max_blocks * page_size.
  *   page_size in {16, 32, 64, 128, 256} else ATTN_ERR_UNSUPPORTED.
  *   workspace: at least attn_decode_workspace_bytes(B, Hq, Hkv,
@@ -299,9 +303,12 @@ attn_status attn_rotate_quantize_fp8_many(const attn_quant_tensor *tensors, int 
 
 /*
  * attn_get_error -- synchronises `stream`, then returns and clears the device
- * error word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a bounded
- * pipeline wait ran out since the last call (its kernel then returned early
- * and its outputs are invalid).  ATTN_ERR_CUDA if the synchronisation failed.
+ * error word of the current device: ATTN_OK, or the first device-side error
+ * since the last call: ATTN_ERR_TIMEOUT if a bounded pipeline wait ran out
+ * (its kernel then returned early and its outputs are invalid),
+ * ATTN_ERR_BAD_INDEX if a decode met a sequence length outside [0, Lmax] or a
+ * block-table entry outside [0, num_pages).  ATTN_ERR_CUDA if the
+ * synchronisation failed.
  */
 attn_status attn_get_error(attn_stream_t stream);
 

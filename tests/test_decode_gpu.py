@@ -80,3 +80,24 @@ def test_decode_more_than_65535_head_pairs():
         Or, Lr = oracle.decode(q, kc, vc, w["seqlens"][b:b + 1].numpy(), 1 / np.sqrt(D))
         check_bf16(o[b:b + 1, 2 * k0:2 * k0 + 16].double().cpu().numpy(), Or,
                    lse[b:b + 1, 2 * k0:2 * k0 + 16].cpu().numpy(), Lr, what=f"decode 72000/36000 b{b} kv{k0}")
+
+
+def test_decode_length_out_of_range_is_reported():
+    """seqlens[b] outside [0, Lmax] is clamped into it (Lmax + 7 -> Lmax,
+    -3 -> 0: O = 0, LSE = -inf) and recorded as ATTN_ERR_BAD_INDEX for
+    attn_get_error; every sequence then matches the oracle at its clamped
+    length, and a later call with good lengths is clean."""
+    import exact_tiled_attention_15_gb300 as eta
+    Lmax = 400
+    w = workloads.make_decode(4, 8, 2, 128, 1, Lmax, seed=32, seqlens=[5, Lmax, 300, 0])
+    dev = torch.device("cuda:0")
+    q, kc, vc = (w[n].to(dev) for n in ("q", "kcache", "vcache"))
+    bad = torch.tensor([5, Lmax + 7, 300, -3], dtype=torch.int32, device=dev)
+    o, lse = eta.decode(q, kc, vc, bad)
+    assert eta.get_error() == eta.ATTN_ERR_BAD_INDEX
+    assert eta.get_error() == 0
+    Or, Lr = oracle.decode(w["q"].double().numpy(), w["kcache"].double().numpy(), w["vcache"].double().numpy(),
+                           w["seqlens"].numpy(), 1 / np.sqrt(128))
+    check_bf16(o.double().cpu().numpy(), Or, lse.cpu().numpy(), Lr, what="decode, clamped lengths")
+    o, lse = eta.decode(q, kc, vc, w["seqlens"].to(dev))
+    assert eta.get_error() == 0

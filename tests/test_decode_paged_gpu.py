@@ -46,3 +46,29 @@ def test_paged_full_size_sampled():
     """64 sequences, 32/8 heads, D=128, lengths in [1024, 8192], 64-row pages
     shuffled through the pool; 6 sequences checked in full."""
     run_case(B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192, ps=64, seed=0, check_rows=[0, 7, 21, 40, 62, 63])
+
+
+def test_paged_bad_block_table_entry_is_reported():
+    """A live block-table entry outside [0, num_pages) (past the pool, or
+    negative): the kernel reads page 0 in its place -- no fault, no read
+    outside the pool -- and records ATTN_ERR_BAD_INDEX for attn_get_error;
+    the other sequences' results are unaffected, and a later call with a good
+    table is clean and correct."""
+    import exact_tiled_attention_15_gb300 as eta
+    ps = 64
+    w = workloads.make_paged_decode(4, 8, 2, 128, 200, 600, ps, seed=31)
+    num_pages = w["k_pages"].shape[0]
+    t = {n: w[n].to(DEV) for n in ("q", "k_pages", "v_pages", "seqlens")}
+    for bad in (num_pages + 5, -1):
+        bt = w["block_table"].clone()
+        bt[2, 1] = bad  # sequence 2 holds at least 200 rows, so its second page is read
+        o, lse = eta.decode_paged(t["q"], t["k_pages"], t["v_pages"], bt.to(DEV), t["seqlens"])
+        assert eta.get_error() == eta.ATTN_ERR_BAD_INDEX
+        assert eta.get_error() == 0  # reported once
+        for b in (0, 1, 3):
+            Or, Lr = oracle.decode_paged(w["q"][b:b + 1].double().numpy(), w["k_pages"].double().numpy(),
+                                         w["v_pages"].double().numpy(), w["block_table"][b:b + 1].numpy(),
+                                         w["seqlens"][b:b + 1].numpy(), ps)
+            check_bf16(o[b:b + 1].double().cpu().numpy(), Or, lse[b:b + 1].cpu().numpy(), Lr,
+                       what=f"paged decode, bad entry {bad} in sequence 2, b={b}")
+    run_case(B=4, Hq=8, Hkv=2, D=128, Lmin=200, Lmax=600, ps=ps, seed=31)
