@@ -457,20 +457,20 @@ def test_hadamard_is_sylvester_closed_form(n):
     np.testing.assert_array_equal(oracle.quant.hadamard(n), expect)
 
 
-def test_rotation_acts_as_hadamard_then_column_signs():
+@pytest.mark.parametrize("D", [64, 128])
+def test_rotation_acts_as_hadamard_then_column_signs(D):
     """The rotation is y = x H_D diag(s) / sqrt(D): the unit row e_i goes to
     s_j (-1)^popcount(i & j) / sqrt(D) in column j.  Signs applied to the rows
     instead (diag(s) H) would give s_i (...) and fail for any non-constant s.
-    Every one of the 128 unit rows is checked (S = 128 rows of one tile)."""
-    D = 128
-    signs = np.random.default_rng(45).integers(0, 2, D) * 2.0 - 1.0
+    Every one of the D unit rows is checked (D rows of one tile)."""
+    signs = np.random.default_rng(45 + D).integers(0, 2, D) * 2.0 - 1.0
     assert 0 < (signs > 0).sum() < D
     x = np.eye(D)[None, None]                                      # row i = e_i
     _, _, y = oracle.rotate_quantize(x, signs)
     i, j = np.meshgrid(np.arange(D), np.arange(D), indexing="ij")
     expect = signs[None, :] * np.where(_popcount(i & j) % 2 == 0, 1.0, -1.0) / np.sqrt(D)
     np.testing.assert_allclose(y[0, 0], expect, rtol=0, atol=1e-15)
-    # the code path: every entry has magnitude 1/sqrt(128), so every code is +-448
+    # the code path: every entry has magnitude 1/sqrt(D), so every code is +-448
     codes, scales, _ = oracle.rotate_quantize(x, signs)
     np.testing.assert_allclose(scales[0, 0, 0, 0], (1 / np.sqrt(D)) / 448.0, rtol=1e-15)
     np.testing.assert_array_equal(oracle.e4m3_decode(codes[0, 0]), 448.0 * np.sign(expect))
