@@ -49,6 +49,15 @@ def test_status_strings(lib):
     assert lib.attn_version().decode().count(".") == 2
 
 
+def test_status_table_matches_header_enum():
+    """The binding's status table is the header's attn_status enum, value for value."""
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    enum = text[text.index("typedef enum"):text.index("} attn_status;")]
+    declared = {int(v): n for n, v in re.findall(r"(ATTN_\w+)\s*=\s*(\d+)", enum)}
+    assert declared == _lib.STATUS
+    assert (_lib.ATTN_ERR_TIMEOUT, _lib.ATTN_ERR_BAD_INDEX) == (4, 7)
+
+
 def p(x):
     return ctypes.c_void_p(x)
 
