@@ -43,9 +43,10 @@ def test_decode_large_logits():
     run_case(B=2, Hq=8, Hkv=2, D=128, Lmin=100, Lmax=200, seed=7, scale=3.0)
 
 
-def test_decode_full_size_sampled():
+def test_decode_full_size_whole_tensor():
     """The benchmark workload (64 sequences, 32/8 heads, D=128, lengths in
-    [1024, 8192]); 8 sequences are checked against the oracle in full."""
+    [1024, 8192]): every sequence, every head, every element of O and every
+    LSE against the oracle."""
     import exact_tiled_attention_15_gb300 as eta
     cfg = workloads.WORKLOADS["gqa_decode"]
     w = workloads.make_decode(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Lmin"], cfg["Lmax"], seed=0)
@@ -56,7 +57,7 @@ def test_decode_full_size_sampled():
     o = o.double().cpu().numpy()
     lse = lse.cpu().numpy()
     assert np.isfinite(o).all()
-    for b in [0, 1, 17, 31, 32, 45, 62, 63]:
+    for b in range(cfg["B"]):
         n = int(w["seqlens"][b])
         Or, Lr = oracle.decode(w["q"][b:b + 1].double().numpy(), w["kcache"][b:b + 1, :, :n].double().numpy(),
                                w["vcache"][b:b + 1, :, :n].double().numpy(), np.array([n]))

@@ -21,9 +21,11 @@ def run_case(B, Hq, Hkv, T, D, Lmin, Lmax, causal=True, seed=0, seqlens=None, ro
     o = o.double().cpu().numpy()
     lse = lse.cpu().numpy()
     sel = list(range(B)) if rows is None else rows
-    Or, Lr = oracle.decode_multi(w["q"][sel].double().numpy(), w["kcache"][sel].double().numpy(),
-                                 w["vcache"][sel].double().numpy(), w["seqlens"][sel].numpy(), causal=causal)
-    check_bf16(o[sel], Or, lse[sel], Lr, what=f"multi decode T={T} {Hq}/{Hkv} causal={causal}")
+    for i in range(0, len(sel), 8):  # eight sequences at a time bound the fp64 copies of the cache
+        s = sel[i:i + 8]
+        Or, Lr = oracle.decode_multi(w["q"][s].double().numpy(), w["kcache"][s].double().numpy(),
+                                     w["vcache"][s].double().numpy(), w["seqlens"][s].numpy(), causal=causal)
+        check_bf16(o[s], Or, lse[s], Lr, what=f"multi decode T={T} {Hq}/{Hkv} causal={causal} b={s[0]}..")
 
 
 @pytest.mark.parametrize("T", [1, 2, 4, 5, 8, 16])
@@ -43,7 +45,7 @@ def test_multi_short_caches():
     run_case(B=5, Hq=8, Hkv=2, T=8, D=128, Lmin=1, Lmax=80, seed=9, seqlens=[0, 1, 3, 8, 80])
 
 
-def test_multi_full_size_sampled():
+def test_multi_full_size_whole_tensor():
     """64 sequences, 32/8 heads, D=128, lengths in [1024, 8192], 4 tokens per
-    sequence (draft length 3 plus one); 6 sequences checked in full."""
-    run_case(B=64, Hq=32, Hkv=8, T=4, D=128, Lmin=1024, Lmax=8192, seed=0, rows=[0, 9, 30, 41, 62, 63])
+    sequence (draft length 3 plus one): every sequence checked in full."""
+    run_case(B=64, Hq=32, Hkv=8, T=4, D=128, Lmin=1024, Lmax=8192, seed=0)

@@ -21,9 +21,9 @@ def run_case(B, Hq, Hkv, D, Lmin, Lmax, ps, seed=0, seqlens=None, check_rows=Non
     o = o.double().cpu().numpy()
     lse = lse.cpu().numpy()
     rows = range(B) if check_rows is None else check_rows
+    kp, vp = w["k_pages"].double().numpy(), w["v_pages"].double().numpy()  # once: the pools are shared
     for b in rows:
-        Or, Lr = oracle.decode_paged(w["q"][b:b + 1].double().numpy(), w["k_pages"].double().numpy(),
-                                     w["v_pages"].double().numpy(), w["block_table"][b:b + 1].numpy(),
+        Or, Lr = oracle.decode_paged(w["q"][b:b + 1].double().numpy(), kp, vp, w["block_table"][b:b + 1].numpy(),
                                      w["seqlens"][b:b + 1].numpy(), ps)
         check_bf16(o[b:b + 1], Or, lse[b:b + 1], Lr, what=f"paged decode ps={ps} b={b}")
 
@@ -42,10 +42,10 @@ def test_paged_ragged_edges():
     run_case(B=7, Hq=8, Hkv=2, D=128, Lmin=1, Lmax=640, ps=64, seed=3, seqlens=[0, 1, 63, 64, 65, 129, 640])
 
 
-def test_paged_full_size_sampled():
+def test_paged_full_size_whole_tensor():
     """64 sequences, 32/8 heads, D=128, lengths in [1024, 8192], 64-row pages
-    shuffled through the pool; 6 sequences checked in full."""
-    run_case(B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192, ps=64, seed=0, check_rows=[0, 7, 21, 40, 62, 63])
+    shuffled through the pool: every sequence checked in full."""
+    run_case(B=64, Hq=32, Hkv=8, D=128, Lmin=1024, Lmax=8192, ps=64, seed=0)
 
 
 def test_paged_bad_block_table_entry_is_reported():
