@@ -21,6 +21,9 @@ Contents
                 from the log-sum-exp).
   quant.py      the e4m3 encoder and the Hadamard-rotate + per-tile e4m3
                 quantisation step of FlashAttention-3's FP8 path.
+  pool.py       the same definitions fanned out over independent (batch,
+                head) units on spawned worker processes, for whole-tensor
+                checks at full size (forward heads; backward KV-head units).
 
 Every function states the passage it follows.  Pins (tests/test_oracle.py)
 check each against invariants, closed forms, brute force and library

@@ -107,3 +107,75 @@ def attention_heads(q, k, v, heads, causal: bool, scale: float | None = None, wo
     workers = min(workers or default_workers(), max(1, len(heads)))
     with HeadPool(q, k, v, workers) as pool:
         return pool.run(heads, causal, scale)
+
+
+# ---------------------------------------------------------------- backward
+# The gradients of one (batch, KV head) unit -- its query-head group with the
+# shared K and V -- are an independent problem too: backward.py computes
+# them by the definition, and dK, dV sum over the group inside that one call,
+# so a unit is never split across workers.
+_WB = {}
+
+
+def _init_bwd(paths):
+    _WB["q"], _WB["k"], _WB["v"], _WB["do"] = (np.load(p, mmap_mode="r") for p in paths)
+
+
+def _one_bwd(task):
+    from .backward import attention_backward
+    idx, b, kv, causal, scale, out_paths = task
+    q, k, v, do = _WB["q"], _WB["k"], _WB["v"], _WB["do"]
+    g = q.shape[1] // k.shape[1]
+    hs = slice(kv * g, (kv + 1) * g)
+    dq, dk, dv, _, _ = attention_backward(q[b:b + 1, hs], k[b:b + 1, kv:kv + 1], v[b:b + 1, kv:kv + 1],
+                                          do[b:b + 1, hs], causal=causal, scale=scale)
+    for arr, path in zip((dq[0], dk[0, 0], dv[0, 0]), out_paths):
+        m = np.load(path, mmap_mode="r+")
+        m[idx] = arr
+        m.flush()
+    return idx
+
+
+def backward_units(q, k, v, do, units, causal: bool, scale: float | None = None, workers: int | None = None):
+    """dQ [n, g, Sq, D], dK [n, Sk, D] and dV [n, Sk, D] (float64) of the
+    listed (b, kv head) units, computed on a pool of at most ``workers``
+    processes; each worker calls ``attention_backward`` on one unit's slice
+    exactly as a serial loop would."""
+    units = [(int(b), int(kv)) for b, kv in units]
+    workers = min(workers or default_workers(), max(1, len(units)))
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    tmp = tempfile.mkdtemp(prefix="oracle_pool_bwd_")
+    try:
+        paths = []
+        for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
+            p = os.path.join(tmp, name + ".npy")
+            np.save(p, np.ascontiguousarray(x))
+            paths.append(p)
+        outs = [os.path.join(tmp, n + ".npy") for n in ("dq", "dk", "dv")]
+        for path, shape in zip(outs, ((len(units), g, Sq, D), (len(units), Sk, D), (len(units), Sk, v.shape[3]))):
+            np.lib.format.open_memmap(path, mode="w+", dtype=np.float64, shape=shape).flush()
+        saved = {n: os.environ.get(n) for n in _BLAS_VARS}
+        try:
+            for n in _BLAS_VARS:
+                os.environ[n] = "1"
+            pool = mp.get_context("spawn").Pool(workers, initializer=_init_bwd, initargs=(paths,))
+        finally:
+            for n, val in saved.items():
+                if val is None:
+                    os.environ.pop(n, None)
+                else:
+                    os.environ[n] = val
+        try:
+            tasks = [(i, b, kv, bool(causal), float(scale), outs) for i, (b, kv) in enumerate(units)]
+            done = pool.map(_one_bwd, tasks, chunksize=1)
+        finally:
+            pool.close()
+            pool.join()
+        assert sorted(done) == list(range(len(units)))
+        return tuple(np.array(np.load(p, mmap_mode="r")) for p in outs)
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)

@@ -523,3 +523,19 @@ def test_process_pool_runs_the_same_definition_per_head():
     for i, (b, h) in enumerate(heads):
         np.testing.assert_array_equal(Op[i], O[b, h])
         np.testing.assert_array_equal(Lp[i], L[b, h])
+
+
+def test_process_pool_backward_units_equal_the_serial_definition():
+    """oracle.pool.backward_units: each (b, KV head) unit's dQ (its query-head
+    group), dK and dV from a spawned worker equal the serial definition's,
+    bit for bit (GQA 4/2, causal with Sq != Sk, units in any order)."""
+    from oracle import pool
+    q, k, v = rand(2, 4, 40, 16, seed=55), rand(2, 2, 57, 16, seed=56), rand(2, 2, 57, 16, seed=57)
+    do = rand(2, 4, 40, 16, seed=58)
+    dq, dk, dv, _, _ = oracle.attention_backward(q, k, v, do, causal=True, scale=0.3)
+    units = [(1, 1), (0, 0), (1, 0)]
+    dqp, dkp, dvp = pool.backward_units(q, k, v, do, units, causal=True, scale=0.3, workers=2)
+    for i, (b, kv) in enumerate(units):
+        np.testing.assert_array_equal(dqp[i], dq[b, 2 * kv:2 * kv + 2])
+        np.testing.assert_array_equal(dkp[i], dk[b, kv])
+        np.testing.assert_array_equal(dvp[i], dv[b, kv])
