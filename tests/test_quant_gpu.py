@@ -145,9 +145,10 @@ def test_all_zero_tile_and_constant_rows():
 
 
 def test_full_size_q_and_fp8_attention_end_to_end():
-    """The FP8 workload's Q (B=2, H=16, S=8192) rotated and quantised on the
-    GPU, checked code by code; then Q, K (rotated) and V (not) feed the FP8
-    attention, checked against the oracle on the dequantised codes."""
+    """The FP8 workload's Q, K (rotated with the same signs) and V (not), each
+    B=2, H=16, S=8192, quantised on the GPU and checked code by code (every
+    code of all three tensors); then they feed the FP8 attention, checked
+    against the oracle on the dequantised codes."""
     import exact_tiled_attention_15_gb300 as eta
     rng = np.random.default_rng(0)
     B, H, S, D = 2, 16, 8192, 128
@@ -161,8 +162,9 @@ def test_full_size_q_and_fp8_attention_end_to_end():
     out = [eta.rotate_quantize_fp8(xs[0].to(DEV), sg), eta.rotate_quantize_fp8(xs[1].to(DEV), sg),
            eta.rotate_quantize_fp8(xs[2].to(DEV), None)]
     assert eta.get_error() == 0
-    n_edge = check(xs[0], signs, out[0][0].cpu(), out[0][1].cpu(), "full-size Q")
-    print(f"full-size Q: {n_edge} of {xs[0].numel()} codes on a rounding boundary")
+    for name, x, sg_, (c, sc) in zip("QKV", xs, (signs, signs, None), out):
+        n_edge = check(x, sg_, c.cpu(), sc.cpu(), f"full-size {name}")
+        print(f"full-size {name}: {n_edge} of {x.numel()} codes on a rounding boundary")
     o, lse = eta.fwd_fp8(out[0][0], out[1][0], out[2][0], out[0][1], out[1][1], out[2][1])
     assert eta.get_error() == 0
     o = o.double().cpu().numpy()
