@@ -24,12 +24,16 @@
 //               (both operands in shared memory, fp32 accumulator in TMEM),
 //               then O_i += P_i V_j with P_i read from TMEM.  Issue order
 //               P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1): while one Q tile's
-//               softmax runs, the tensor core works on the other tile;
+//               softmax runs, the tensor core works on the other tile
+//               (FP8: P_i from shared memory, order S_0(j+1), S_1(j+1),
+//               P_0 V_j, P_1 V_j, each S once its tile's softmax has read
+//               the previous one);
 //   warps 0-3   softmax of Q tile 0, one thread per query row (TMEM lane);
 //   warps 4-7   softmax of Q tile 1.
 // The softmax uses the packed fp32x2 FMA/ADD and three-input max of sm_100+.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 after it.
-// P_i overwrites the first columns of S_i.  The running max only moves when
+// P_i overwrites the first columns of S_i (FP8: P_i in shared memory, two
+// buffers per Q tile after the V ring).  The running max only moves when
 // the new maximum exceeds it by more than a threshold (log2 units), so O is
 // rescaled rarely.
 //
@@ -78,6 +82,8 @@ struct Bf16 {
   // tile later than its own commit would), saving a commit per key tile;
   // needs equal ring depths.
   static constexpr bool kKRelByV = false;
+  // P_i goes back into S_i's TMEM columns, so S_i(j+1) waits for P_i V_j.
+  static constexpr bool kPSmem = false;
 };
 
 struct Fp8 {
@@ -97,6 +103,14 @@ struct Fp8 {
   // loads ahead (four measured no faster, 160 KB of shared memory).
   static constexpr int kNSK = 3, kNSV = 3;
   static constexpr bool kKRelByV = true;
+  // P_i goes to shared memory (two 16 KB buffers per Q tile) and P.V reads
+  // both operands from there.  S_i's columns are free as soon as the softmax
+  // has read them, so S_i(j+1) runs during softmax_i(j) instead of after
+  // P_i V_j: the softmax phases follow each other without waiting for the
+  // products, which is what the FP8 tile (products half as long as bf16's,
+  // as many exponentials) is bound by.  bf16 keeps P in TMEM: its products
+  // already fill the tensor core and shared memory.
+  static constexpr bool kPSmem = true;
 };
 
 template <class T, int D>
@@ -108,8 +122,10 @@ struct Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQT * TILE;
   static constexpr int OFF_V = OFF_K + NSK * TILE;
-  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 3 * NQT + 2;
+  static constexpr int NP = T::kPSmem ? 2 * NQT : 0;  // P buffers in shared memory, two per Q tile
+  static constexpr int OFF_P = OFF_V + NSV * TILE;
+  static constexpr int OFF_BAR = OFF_P + NP * HALF;
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 4 * NQT + 2;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
   static constexpr int P_REGS = BN * T::kElem / 4;  // 32-bit TMEM columns holding one P row
@@ -121,6 +137,8 @@ struct Cfg {
   static constexpr uint32_t IDESC_PV =
       (1u << 4) | T::kTypeBits | (1u << 16) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
   static_assert(NH >= 1, "tile rows must span at least one 128-byte slab");
+  static_assert(!T::kPSmem || BN * T::kElem == 128, "a P row in shared memory is one 128-byte swizzle row");
+  static_assert(!T::kPSmem || T::kKRelByV, "with P in shared memory K slots go back with the V release");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(NQT * BN + NQT * D <= (int)TMEM_COLS, "TMEM budget");
 };
@@ -139,8 +157,9 @@ struct Params {
   unsigned *err;
 };
 
+// both operands in shared memory
 template <class T>
-__device__ __forceinline__ void mma_qk(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_smem(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if constexpr (T::kFp8) mma_ss_f8(d, a, b, idesc, acc);
   else mma_ss(d, a, b, idesc, acc);
 }
@@ -164,7 +183,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *k_full = bars + 1, *k_empty = k_full + NSK;
   uint64_t *v_full = k_empty + NSK, *v_empty = v_full + NSV;
   uint64_t *s_full = v_empty + NSV, *p_full = s_full + NQT, *o_full = p_full + NQT;
-  uint64_t *done_bar = o_full + NQT;
+  uint64_t *s_free = o_full + NQT;  // P in shared memory: the softmax has read S_i
+  uint64_t *done_bar = s_free + NQT;
   uint64_t *never = done_bar + 1;  // test hook: no thread ever arrives on it
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEMPTR);
 
@@ -222,10 +242,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int i = 0; i < NQT; ++i) {  // p_full: one arrival per softmax warp
+    for (int i = 0; i < NQT; ++i) {  // p_full, s_free: one arrival per softmax warp
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], BM / 32);
       mbar_init(&o_full[i], 1);
+      mbar_init(&s_free[i], BM / 32);
     }
     mbar_init(done_bar, 1);
     mbar_init(never, 1);
@@ -297,7 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / T::kMmaK; ++kk) {
           const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_qk<T>(tmem + C::col_s(i), sdesc_add(dq, o), sdesc_add(dk, o), C::IDESC_QK, kk > 0);
+          mma_smem<T>(tmem + C::col_s(i), sdesc_add(dq, o), sdesc_add(dk, o), C::IDESC_QK, kk > 0);
         }
         tc_commit(&s_full[i]);
       };
@@ -323,21 +344,66 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (nkv_t[i] > 0) issue_s(i, 0);
         if (!T::kKRelByV) tc_commit(&k_empty[0]);
       }
-      for (int j = 0; ok && j < nkv; ++j) {
-        const bool next = j + 1 < nkv;
-        if (!mbar_wait(&v_full[j % NSV], (j / NSV) & 1, p.timeout_ns, p.err)) break;
-        tc_fence_after();
-        if (j < nkv_t[0] && !issue_pv(0, j)) break;
-        if (next) {
-          if (!mbar_wait(&k_full[(j + 1) % NSK], ((j + 1) / NSK) & 1, p.timeout_ns, p.err)) break;
+      if constexpr (T::kPSmem) {
+        // O_i += P_i V_j with P_i in shared memory (buffer j & 1, K-major,
+        // 128-byte swizzle: 32 keys = 32 bytes of each row per instruction).
+        // Issue order S_0(j+1), S_1(j+1), P_0 V_j, P_1 V_j: each S as soon as
+        // its tile's softmax has read the previous one.  P_i V_j precedes
+        // S_i(j+2), so the softmax's wait for S_i(j+2) also tells it that
+        // buffer j & 1 is free again.
+        const uint64_t dp0 = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
+        auto issue_pv_smem = [&](int i, int j) -> bool {
+          if (!mbar_wait(&p_full[i], j & 1, p.wait_ns, p.err)) return false;
           tc_fence_after();
-          if (j + 1 < nkv_t[0]) issue_s(0, j + 1);
+          const uint64_t dp = sdesc_add(dp0, (2 * i + (j & 1)) * HALF);
+          const uint64_t dv = sdesc_add(dv0, (j % NSV) * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < BN / T::kMmaK; ++kk)
+            mma_smem<T>(tmem + C::col_o(i), sdesc_add(dp, kk * T::kMmaK * T::kElem),
+                        sdesc_add(dv, kk * T::kMmaK * 128), C::IDESC_PV, (j > 0 || kk > 0));
+          if (j + 1 == nkv_t[i]) tc_commit(&o_full[i]);
+          return true;
+        };
+        for (int j = 0; ok && j < nkv; ++j) {
+          if (j + 1 < nkv) {
+            if (!mbar_wait(&k_full[(j + 1) % NSK], ((j + 1) / NSK) & 1, p.timeout_ns, p.err)) break;
+            tc_fence_after();
+            bool fine = true;
+#pragma unroll
+            for (int i = 0; i < NQT; ++i) {
+              if (fine && j + 1 < nkv_t[i]) {
+                fine = mbar_wait(&s_free[i], j & 1, p.wait_ns, p.err);
+                if (fine) {
+                  tc_fence_after();
+                  issue_s(i, j + 1);
+                }
+              }
+            }
+            if (!fine) break;
+          }
+          if (!mbar_wait(&v_full[j % NSV], (j / NSV) & 1, p.timeout_ns, p.err)) break;
+          tc_fence_after();
+          if (j < nkv_t[0] && !issue_pv_smem(0, j)) break;
+          if (j < nkv_t[1] && !issue_pv_smem(1, j)) break;
+          tc_commit(&v_empty[j % NSV]);  // also frees K slot j (K_j's last product, S_1(j), came before)
         }
-        if (j < nkv_t[1] && !issue_pv(1, j)) break;
-        tc_commit(&v_empty[j % NSV]);
-        if (next) {
-          if (j + 1 < nkv_t[1]) issue_s(1, j + 1);
-          if (!T::kKRelByV) tc_commit(&k_empty[(j + 1) % NSK]);
+      } else {
+        for (int j = 0; ok && j < nkv; ++j) {
+          const bool next = j + 1 < nkv;
+          if (!mbar_wait(&v_full[j % NSV], (j / NSV) & 1, p.timeout_ns, p.err)) break;
+          tc_fence_after();
+          if (j < nkv_t[0] && !issue_pv(0, j)) break;
+          if (next) {
+            if (!mbar_wait(&k_full[(j + 1) % NSK], ((j + 1) / NSK) & 1, p.timeout_ns, p.err)) break;
+            tc_fence_after();
+            if (j + 1 < nkv_t[0]) issue_s(0, j + 1);
+          }
+          if (j < nkv_t[1] && !issue_pv(1, j)) break;
+          tc_commit(&v_empty[j % NSV]);
+          if (next) {
+            if (j + 1 < nkv_t[1]) issue_s(1, j + 1);
+            if (!T::kKRelByV) tc_commit(&k_empty[(j + 1) % NSK]);
+          }
         }
       }
       // every product issued above has completed before the CTA moves on
@@ -392,6 +458,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       uint32_t s[128];
       tmem_ld128(taddr + s_col, s);
+      if constexpr (T::kPSmem) {  // S_i's columns may take the next key tile's scores now
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[i]);
+      }
       const int kb = j * BN;
       const bool masked = kb + BN - 1 > lim;  // diagonal or ragged tile
       if (masked) {
@@ -470,17 +541,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float back = T::kFp8 ? fast_exp2(-e_off) : 1.f;
       l = l * alpha + rs * back;
       l_o = l_o * alpha + (rs + (pm_r - pm)) * back;
+      if constexpr (T::kPSmem) {
+        // row r of buffer j & 1: 16-byte chunk c at position c ^ (r & 7) (the
+        // 128-byte swizzle); eight consecutive rows cover all 32 banks
+        uint8_t *prow = smem + C::OFF_P + (2 * i + (j & 1)) * HALF + r * 128;
 #pragma unroll
-      for (int c = 0; c < C::P_REGS / 32; ++c) {
-        uint32_t chunk[32];
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) chunk[e] = pk[c * 32 + e];
-        tmem_st32(taddr + s_col + c * 32, chunk);
+        for (int c = 0; c < C::P_REGS / 32; ++c) {
+          uint32_t chunk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) chunk[e] = pk[c * 32 + e];
+          tmem_st32(taddr + s_col + c * 32, chunk);
+        }
       }
       // Rescale O_i by alpha once P_{j-1} V_{j-1} has landed (warp-uniform).
+      // With P in TMEM and no per-tile o_full, S_i(j) (issued after it)
+      // implies it; with P in shared memory S_i(j) may come first, and the V
+      // release of key tile j-1 (committed after both tiles' P V_{j-1}) does.
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (T::kOFullEachTile &&
-            !__all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.wait_ns, p.err))) {
+        bool landed = true;
+        if constexpr (T::kOFullEachTile)
+          landed = __all_sync(0xffffffffu, mbar_wait(&o_full[i], (j - 1) & 1, p.wait_ns, p.err));
+        else if constexpr (T::kPSmem)
+          landed = __all_sync(0xffffffffu,
+                              mbar_wait(&v_empty[(j - 1) % NSV], ((j - 1) / NSV) & 1, p.wait_ns, p.err));
+        if (!landed) {
           tmem_st_wait();  // no store of P may still be in flight when the CTA ends
           ok = false;
           break;
@@ -495,6 +584,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st32(taddr + o_col + c * 32, ov);
         }
       }
+      if constexpr (T::kPSmem) fence_proxy_async_smem();  // P's stores before the tensor core reads them
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
