@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
           mma_smem<T>(tmem + C::col_s(i), sdesc_add(dq, o), sdesc_add(dk, o), C::IDESC_QK, kk > 0);
         }
-        tc_commit(&s_full[i]);
+        if (!T::kPSmem) tc_commit(&s_full[i]);
       };
       // O_i += P_i V_j: P from TMEM (8 columns per instruction), V MN-major
       // (rows = keys; 128-byte slabs of the head dimension HALF bytes apart)
@@ -342,14 +342,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < NQT; ++i)
           if (nkv_t[i] > 0) issue_s(i, 0);
+        if (T::kPSmem) tc_commit(&s_full[0]);  // one signal for both tiles' scores
         if (!T::kKRelByV) tc_commit(&k_empty[0]);
       }
       if constexpr (T::kPSmem) {
         // O_i += P_i V_j with P_i in shared memory (buffer j & 1, K-major,
         // 128-byte swizzle: 32 keys = 32 bytes of each row per instruction).
         // Issue order S_0(j+1), S_1(j+1), P_0 V_j, P_1 V_j: each S as soon as
-        // its tile's softmax has read the previous one.  P_i V_j precedes
-        // S_i(j+2), so the softmax's wait for S_i(j+2) also tells it that
+        // its tile's softmax has read the previous one, and one commit on
+        // s_full[0] for both (a commit costs ~74 cycles of the tensor pipe;
+        // tile 0's softmax waits the ~120 ns of S_1 more).  P_i V_j precedes
+        // S_i(j+2), so the softmax's wait for S(j+2) also tells it that
         // buffer j & 1 is free again.
         const uint64_t dp0 = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
         auto issue_pv_smem = [&](int i, int j) -> bool {
@@ -380,6 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
             if (!fine) break;
+            tc_commit(&s_full[0]);
           }
           if (!mbar_wait(&v_full[j % NSV], (j / NSV) & 1, p.timeout_ns, p.err)) break;
           tc_fence_after();
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           vs_next = __ldg(&p.v_scale[(size_t)zk * p.nkt + j + 1]);
         }
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[i], j & 1, p.wait_ns, p.err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[T::kPSmem ? 0 : i], j & 1, p.wait_ns, p.err))) {
         ok = false;
         break;
       }
