@@ -125,7 +125,7 @@ struct Cfg {
   static constexpr int NP = T::kPSmem ? 2 * NQT : 0;  // P buffers in shared memory, two per Q tile
   static constexpr int OFF_P = OFF_V + NSV * TILE;
   static constexpr int OFF_BAR = OFF_P + NP * HALF;
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 4 * NQT + 2;
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 5 * NQT + 2;
   static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;
   static constexpr int P_REGS = BN * T::kElem / 4;  // 32-bit TMEM columns holding one P row
@@ -182,7 +182,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1, *k_empty = k_full + NSK;
   uint64_t *v_full = k_empty + NSK, *v_empty = v_full + NSV;
-  uint64_t *s_full = v_empty + NSV, *p_full = s_full + NQT, *o_full = p_full + NQT;
+  // p_full: one per Q tile; with P in shared memory two per Q tile (key tile
+  // parity), since a tile's softmax may then finish key tile j + 1 before the
+  // issuing thread has waited for its P of key tile j
+  uint64_t *s_full = v_empty + NSV, *p_full = s_full + NQT, *o_full = p_full + 2 * NQT;
   uint64_t *s_free = o_full + NQT;  // P in shared memory: the softmax has read S_i
   uint64_t *done_bar = s_free + NQT;
   uint64_t *never = done_bar + 1;  // test hook: no thread ever arrives on it
@@ -244,7 +247,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < NQT; ++i) {  // p_full, s_free: one arrival per softmax warp
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], BM / 32);
+      mbar_init(&p_full[2 * i], BM / 32);
+      mbar_init(&p_full[2 * i + 1], BM / 32);
       mbar_init(&o_full[i], 1);
       mbar_init(&s_free[i], BM / 32);
     }
@@ -355,41 +359,96 @@ __global__ void __launch_bounds__(THREADS, 1)
         // S_i(j+2), so the softmax's wait for S(j+2) also tells it that
         // buffer j & 1 is free again.
         const uint64_t dp0 = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
-        auto issue_pv_smem = [&](int i, int j) -> bool {
-          if (!mbar_wait(&p_full[i], j & 1, p.wait_ns, p.err)) return false;
-          tc_fence_after();
+        // The issuing thread sets the pace here, so its loop carries as few
+        // instructions as possible: ring slots and phases as counters, and
+        // the key tiles both Q tiles visit (now and next) in a loop of their
+        // own without per-tile checks.  K_{j+1} and V_j share the ring depth.
+        static_assert(NSK == NSV, "one slot counter for both rings");
+        int ks = 1 % NSK, kph = NSK == 1 ? 1 : 0;  // slot and phase of K_{j+1}
+        int vsl = 0, vph = 0;                      // slot and phase of V_j
+        auto step = [](int &slot, int &ph) {
+          if (++slot == NSK) {
+            slot = 0;
+            ph ^= 1;
+          }
+        };
+        auto wait_p = [&](int i, int j) -> bool {
+          return mbar_wait(&p_full[2 * i + (j & 1)], (j >> 1) & 1, p.wait_ns, p.err);
+        };
+        auto issue_s_slot = [&](int i) {
+          const uint64_t dq = sdesc_add(dq0, i * C::TILE), dk = sdesc_add(dk0, ks * C::TILE);
+#pragma unroll
+          for (int kk = 0; kk < D / T::kMmaK; ++kk) {
+            const uint32_t o = (kk >> 2) * HALF + (kk & 3) * 32;
+            mma_smem<T>(tmem + C::col_s(i), sdesc_add(dq, o), sdesc_add(dk, o), C::IDESC_QK, kk > 0);
+          }
+        };
+        auto issue_pv_smem = [&](int i, int j) {
           const uint64_t dp = sdesc_add(dp0, (2 * i + (j & 1)) * HALF);
-          const uint64_t dv = sdesc_add(dv0, (j % NSV) * C::TILE);
+          const uint64_t dv = sdesc_add(dv0, vsl * C::TILE);
 #pragma unroll
           for (int kk = 0; kk < BN / T::kMmaK; ++kk)
             mma_smem<T>(tmem + C::col_o(i), sdesc_add(dp, kk * T::kMmaK * T::kElem),
                         sdesc_add(dv, kk * T::kMmaK * 128), C::IDESC_PV, (j > 0 || kk > 0));
-          if (j + 1 == nkv_t[i]) tc_commit(&o_full[i]);
-          return true;
         };
-        for (int j = 0; ok && j < nkv; ++j) {
+        const int jb = max(0, min(nkv_t[0], nkv_t[1]) - 1);  // j < jb: both tiles visit j and j + 1
+        int j = 0;
+        for (; ok && j < jb; ++j) {
+          ok = mbar_wait(&k_full[ks], kph, p.timeout_ns, p.err) && mbar_wait(&s_free[0], j & 1, p.wait_ns, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s_slot(0);
+          if (!(ok = mbar_wait(&s_free[1], j & 1, p.wait_ns, p.err))) break;
+          tc_fence_after();
+          issue_s_slot(1);
+          tc_commit(&s_full[0]);
+          step(ks, kph);
+          if (!(ok = mbar_wait(&v_full[vsl], vph, p.timeout_ns, p.err) && wait_p(0, j))) break;
+          tc_fence_after();
+          issue_pv_smem(0, j);
+          if (!(ok = wait_p(1, j))) break;
+          tc_fence_after();
+          issue_pv_smem(1, j);
+          tc_commit(&v_empty[vsl]);  // also frees K slot j (K_j's last product, S_1(j), came before)
+          step(vsl, vph);
+        }
+        // the last key tiles: a tile may stop earlier (causal) or see no key at all
+        for (; ok && j < nkv; ++j) {
           if (j + 1 < nkv) {
-            if (!mbar_wait(&k_full[(j + 1) % NSK], ((j + 1) / NSK) & 1, p.timeout_ns, p.err)) break;
+            if (!(ok = mbar_wait(&k_full[ks], kph, p.timeout_ns, p.err))) break;
             tc_fence_after();
-            bool fine = true;
 #pragma unroll
             for (int i = 0; i < NQT; ++i) {
-              if (fine && j + 1 < nkv_t[i]) {
-                fine = mbar_wait(&s_free[i], j & 1, p.wait_ns, p.err);
-                if (fine) {
+              // a tile whose last key tile is j must also have read S(j)
+              // before s_full completes the phase of S(j+1): a waiter two
+              // phases behind would read the parity wrongly
+              if (ok && j < nkv_t[i]) {
+                ok = mbar_wait(&s_free[i], j & 1, p.wait_ns, p.err);
+                if (ok && j + 1 < nkv_t[i]) {
                   tc_fence_after();
-                  issue_s(i, j + 1);
+                  issue_s_slot(i);
                 }
               }
             }
-            if (!fine) break;
+            if (!ok) break;
             tc_commit(&s_full[0]);
+            step(ks, kph);
           }
-          if (!mbar_wait(&v_full[j % NSV], (j / NSV) & 1, p.timeout_ns, p.err)) break;
-          tc_fence_after();
-          if (j < nkv_t[0] && !issue_pv_smem(0, j)) break;
-          if (j < nkv_t[1] && !issue_pv_smem(1, j)) break;
-          tc_commit(&v_empty[j % NSV]);  // also frees K slot j (K_j's last product, S_1(j), came before)
+          if (!(ok = mbar_wait(&v_full[vsl], vph, p.timeout_ns, p.err))) break;
+#pragma unroll
+          for (int i = 0; i < NQT; ++i) {
+            if (ok && j < nkv_t[i]) {
+              ok = wait_p(i, j);
+              if (ok) {
+                tc_fence_after();
+                issue_pv_smem(i, j);
+                if (j + 1 == nkv_t[i]) tc_commit(&o_full[i]);
+              }
+            }
+          }
+          if (!ok) break;
+          tc_commit(&v_empty[vsl]);
+          step(vsl, vph);
         }
       } else {
         for (int j = 0; ok && j < nkv; ++j) {
@@ -592,7 +651,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[i]);
+      if (lane == 0) mbar_arrive(&p_full[T::kPSmem ? 2 * i + (j & 1) : i]);
     }
     // ---------------------------------------------------------- epilogue
     if (ok && my_nkv > 0)
