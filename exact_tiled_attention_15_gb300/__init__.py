@@ -16,4 +16,4 @@
 All of them call the C ABI of libattn.so (include/attn.h) on the current CUDA
 stream; the library is loaded on first use and a missing library raises.
 """
-from ._lib import ATTN_ERR_BAD_INDEX, ATTN_ERR_TIMEOUT, STATUS, AttnError, bwd, debug_stall_role_waits, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, fwd_host, fwd_host_workspace_bytes, get_error, lib, rotate_quantize_fp8, rotate_quantize_fp8_many, version  # noqa: F401
+from ._lib import ATTN_ERR_BAD_INDEX, ATTN_ERR_TIMEOUT, STATUS, AttnError, bwd, debug_skew_roles, debug_stall_role_waits, decode, decode_multi, decode_noalloc, decode_paged, decode_workspace_bytes, fwd, fwd_fp8, fwd_host, fwd_host_workspace_bytes, get_error, lib, rotate_quantize_fp8, rotate_quantize_fp8_many, version  # noqa: F401

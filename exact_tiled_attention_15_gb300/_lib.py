@@ -40,6 +40,7 @@ SIGNATURES = {
     "attn_rotate_quantize_fp8_many": (_I, [_P, _I, _P, _I, _P]),
     "attn_get_error": (_I, [_P]),
     "attn_debug_stall_role_waits": (None, [_I]),
+    "attn_debug_skew_roles": (None, [_I]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
     "attn_version": (ctypes.c_char_p, []),
 }
@@ -452,6 +453,12 @@ def debug_stall_role_waits(enable: bool) -> None:
     """Test hook: later forward/backward calls wait for a signal nothing gives
     (bounded at 1 ms) and report ATTN_ERR_TIMEOUT; False restores them."""
     lib().attn_debug_stall_role_waits(1 if enable else 0)
+
+
+def debug_skew_roles(enable: bool) -> None:
+    """Test hook: later FP8 forward calls run with fixed delays in two warp
+    roles, so the others run ahead of them; False restores them."""
+    lib().attn_debug_skew_roles(1 if enable else 0)
 
 
 def version() -> str:

@@ -32,6 +32,10 @@ uint64_t role_wait_ns() {
 }
 int debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 
+// attn_debug_skew_roles: when set, forward kernels that support it run with
+// fixed delays in some warp roles, so that others run ahead of them.
+std::atomic<int> g_debug_skew{0};
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -158,6 +162,7 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
   a.timeout_ns = kDefaultTimeoutNs;
   a.wait_ns = role_wait_ns();
   a.stall = debug_stall();
+  a.skew = g_debug_skew.load(std::memory_order_relaxed);
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_fwd_bf16(a, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
@@ -366,6 +371,7 @@ attn_status attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8
   a.timeout_ns = kDefaultTimeoutNs;
   a.wait_ns = role_wait_ns();
   a.stall = debug_stall();
+  a.skew = g_debug_skew.load(std::memory_order_relaxed);
   a.err = error_word();
   if (!a.err) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_fwd_fp8(a, tq, tk, tv, reinterpret_cast<cudaStream_t>(stream)));
@@ -512,6 +518,8 @@ attn_status attn_rotate_quantize_fp8_many(const attn_quant_tensor *tensors, int 
 }
 
 void attn_debug_stall_role_waits(int enable) { g_debug_stall.store(enable ? 1 : 0, std::memory_order_relaxed); }
+
+void attn_debug_skew_roles(int enable) { g_debug_skew.store(enable ? 1 : 0, std::memory_order_relaxed); }
 
 attn_status attn_get_error(attn_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -170,7 +170,18 @@ __device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a_tmem, uint64_t b, 
   else mma_ts(d, a_tmem, b, idesc, acc);
 }
 
-template <class T, int D>
+// Test hook, compiled only into the kSkew instantiation: a fixed 20 us delay
+// of one warp role, so that the others run ahead of it.
+__device__ __forceinline__ void skew_delay() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 20000ull) {
+  }
+}
+
+// kSkew: the issuing thread pauses after each S commit and tile 0's softmax
+// before each wait for S, so the other tile's softmax and the issuing thread
+// get ahead of it (the barrier-phase cases of the P-in-shared-memory order).
+template <class T, int D, bool kSkew = false>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, Params p) {
@@ -403,6 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           issue_s_slot(1);
           tc_commit(&s_full[0]);
           step(ks, kph);
+          if constexpr (kSkew) skew_delay();
           if (!(ok = mbar_wait(&v_full[vsl], vph, p.timeout_ns, p.err) && wait_p(0, j))) break;
           tc_fence_after();
           issue_pv_smem(0, j);
@@ -433,6 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) break;
             tc_commit(&s_full[0]);
             step(ks, kph);
+            if constexpr (kSkew) skew_delay();
           }
           if (!(ok = mbar_wait(&v_full[vsl], vph, p.timeout_ns, p.err))) break;
 #pragma unroll
@@ -513,6 +526,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           ks_next = __ldg(&p.k_scale[(size_t)zk * p.nkt + j + 1]);
           vs_next = __ldg(&p.v_scale[(size_t)zk * p.nkt + j + 1]);
         }
+      }
+      if constexpr (kSkew) {
+        if (i == 0) skew_delay();
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[T::kPSmem ? 0 : i], j & 1, p.wait_ns, p.err))) {
         ok = false;
@@ -732,10 +748,14 @@ cudaError_t launch(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &t
   p.stall = a.stall;
   p.err = a.err;
   if ((long)p.nqb * a.B * a.Hq > 0x7fffffffL) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  auto kern = fwd_kernel<T, D, false>;
+  if constexpr (T::kPSmem) {  // the skew hook exists for the P-in-shared-memory order only
+    if (a.skew) kern = fwd_kernel<T, D, true>;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((long)p.nqb * a.B * a.Hq));
-  fwd_kernel<T, D><<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, p);
+  kern<<<grid, THREADS, C::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,7 @@ struct FwdArgs {
   uint64_t timeout_ns;  // waits on copies and on a CTA's own tensor-core work
   uint64_t wait_ns;     // waits of one warp role on another inside a CTA
   int stall;            // test hook: the softmax first waits for a signal nothing gives
+  int skew;             // test hook: fixed delays that let one warp role run ahead of another
   unsigned *err;
 };
 

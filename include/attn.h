@@ -333,6 +333,22 @@ attn_status attn_get_error(attn_stream_t stream);
  */
 void attn_debug_stall_role_waits(int enable);
 
+/*
+ * attn_debug_skew_roles -- test hook for the synchronisation of the FP8
+ * prefill forward (attn_fwd_fp8; no page defines it).  There the issuing
+ * thread asks for the next key tile's scores before it consumes the current
+ * probabilities, so a warp role may run up to a key tile ahead of another.
+ * With enable != 0, every attn_fwd_fp8 call made afterwards runs a build of
+ * the kernel in which the issuing thread pauses 20 us after each request for
+ * scores and the softmax warps of each CTA's first query tile pause 20 us
+ * before each wait for scores, so that the other roles get as far ahead as
+ * the protocol allows.  Results and error reporting are those of a normal
+ * call (only slower); a protocol that miscounted a barrier phase would show
+ * as ATTN_ERR_TIMEOUT from attn_get_error().  enable = 0 restores normal
+ * operation.  Process-wide; for tests only.
+ */
+void attn_debug_skew_roles(int enable);
+
 /* Human-readable name of a status code (static string). */
 const char *attn_status_str(attn_status status);
 

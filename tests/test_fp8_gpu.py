@@ -120,3 +120,29 @@ def test_fp8_full_size_whole_tensor():
     assert max(per_head) <= FP8_REL_RMS
     print(f"fp8_prefill, whole tensor (32 heads): relative RMS {rr:.4f} (per head max {max(per_head):.4f}), "
           f"max|dLSE| {dl:.3g}")
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1000, 1000), (700, 1300), (1300, 700)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_skewed_roles(Sq, Sk, causal):
+    """The FP8 kernel issues the next key tile's scores before it consumes the
+    current probabilities, so its warp roles may drift up to a key tile apart.
+    With attn_debug_skew_roles the issuing thread pauses after each request
+    for scores and the first query tile's softmax before each wait for them:
+    the other tile's softmax finishes its next probabilities before the
+    issuing thread asks for the current ones, and under the causal mask (the
+    first tile stopping a key tile early) the second tile's next scores are
+    requested while the first tile still sleeps.  A miscounted barrier phase
+    would show as a wait that runs out; the results must be those of the
+    oracle, as without the delays."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = fp8_inputs(workloads.make_fp8_prefill(1, 4, 2, Sq, Sk, 128, seed=Sq * 3 + Sk))
+    eta.debug_skew_roles(True)
+    try:
+        o, lse = gpu_fp8(w, causal)
+    finally:
+        eta.debug_skew_roles(False)
+    Or, Lr = oracle.attention(deq(w, "q"), deq(w, "k"), deq(w, "v"), causal=causal)
+    check(o, lse, Or, Lr, f"fp8 skewed {Sq}x{Sk} causal={causal}")
+    o2, lse2 = gpu_fp8(w, causal)  # the normal build, same inputs: the same bits
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
