@@ -95,12 +95,13 @@ struct Fp8 {
   static constexpr uint32_t kTypeBits = 0u;  // A and B e4m3
   // A commit costs ~71 cycles of the tensor pipe, and an FP8 key tile has
   // only ~1024 cycles of products: the per-tile o_full commits are dropped.
-  // The O rescale of tile j needs P_i V_{j-1} landed, which S_i(j) implies
-  // (it was issued after it, and the softmax has waited for S_i(j)).
+  // The O rescale of tile j needs P_i V_{j-1} landed; the V release of key
+  // tile j-1, committed after both tiles' P V_{j-1}, says so.
   static constexpr bool kOFullEachTile = false;
   // For the same reason K slots go back with the V release: K_j is free once
   // P_1 V_j is done (S_1(j) came before it).  Three stages of each keep the
-  // loads ahead (four measured no faster, 160 KB of shared memory).
+  // loads ahead (four measured no faster: 224 KB of shared memory with the P
+  // buffers, against 198 KB).
   static constexpr int kNSK = 3, kNSV = 3;
   static constexpr bool kKRelByV = true;
   // P_i goes to shared memory (two 16 KB buffers per Q tile) and P.V reads
