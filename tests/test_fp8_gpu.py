@@ -146,3 +146,22 @@ def test_fp8_skewed_roles(Sq, Sk, causal):
     check(o, lse, Or, Lr, f"fp8 skewed {Sq}x{Sk} causal={causal}")
     o2, lse2 = gpu_fp8(w, causal)  # the normal build, same inputs: the same bits
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,causal", [(2, 16, 16, 8192, False), (1, 8, 2, 4100, True)])
+def test_fp8_skewed_roles_long_sequences_bit_equal(B, Hq, Hkv, S, causal):
+    """The skewed-role build over many key tiles per CTA (64 at the FP8
+    benchmark size; a causal GQA case whose two Q tiles stop a key tile
+    apart): the rings wrap many times while the roles sit as far apart as the
+    protocol lets them, and the output must be the normal build's, bit for
+    bit (the normal build is compared with the oracle at these sizes by the
+    whole-tensor tests)."""
+    import exact_tiled_attention_15_gb300 as eta
+    w = fp8_inputs(workloads.make_fp8_prefill(B, Hq, Hkv, S, S, 128, seed=S + B))
+    o, lse = gpu_fp8(w, causal)
+    eta.debug_skew_roles(True)
+    try:
+        o2, lse2 = gpu_fp8(w, causal)
+    finally:
+        eta.debug_skew_roles(False)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
